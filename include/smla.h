@@ -1,0 +1,141 @@
+/*
+ * smla.h -- C ABI of libsmla: the FP8 lightning indexer, per-token top-k and
+ * sparse MLA prefill attention for GB300 (sm_103a).
+ *
+ * Every entry point takes plain device pointers and sizes, validates them on
+ * the host, enqueues its kernels asynchronously on `stream` and returns an
+ * smla_status_t.  The caller owns every buffer; the library allocates no
+ * device memory.  No C++ exception crosses this boundary.  A call that
+ * returns anything but SMLA_OK has enqueued nothing (except SMLA_ERR_CUDA,
+ * where a launch was attempted and failed); smla_last_error() then holds a
+ * message for the calling thread.
+ *
+ * Errors found on the device (an index or page id outside the pool, a
+ * pipeline wait that gave up) are recorded in a per-device error word
+ * instead of faulting; the kernel that found them skips the offending
+ * access and finishes.  smla_check_device_errors() reads and clears that
+ * word.  Outputs of a call that recorded a device error are unspecified.
+ *
+ * Layouts are row-major and dense unless a stride is given.  "e4m3" is the
+ * float8_e4m3fn byte format; "bf16" is bfloat16 bits.  Device pointers must
+ * be 16-byte aligned.
+ */
+#ifndef SMLA_H_
+#define SMLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SMLA_OK = 0,
+  SMLA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer */
+  SMLA_ERR_UNSUPPORTED = 2,  /* valid but outside the shapes this build implements */
+  SMLA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+  SMLA_ERR_TIMEOUT = 4,      /* a device pipeline wait gave up (device error word) */
+  SMLA_ERR_DEVICE_CHECK = 5  /* an index / page id was out of range (device error word) */
+} smla_status_t;
+
+enum { SMLA_BF16 = 0, SMLA_E4M3 = 1 };
+
+/* Ragged batch of B sequences over a paged cache (all pointers on the device).
+ * Sequence b owns query tokens cu_q[b] .. cu_q[b+1]-1 and kv_len[b] cached
+ * tokens; its q_len = cu_q[b+1]-cu_q[b] new tokens are the LAST q_len cached
+ * positions, so its token i sits at pos = kv_len[b] - q_len + i and may
+ * attend to logical keys 0..pos.  Logical key j of sequence b is physical
+ * row page_table[b*max_pages + j/page_size]*page_size + j%page_size.
+ * T = cu_q[B] (passed on the host so that no call reads device memory to
+ * size its grid).  Requires q_len <= kv_len for every sequence. */
+typedef struct {
+  const int32_t* cu_q;        /* [B+1] */
+  const int32_t* kv_len;      /* [B] */
+  const int32_t* page_table;  /* [B, max_pages] physical page ids */
+  int32_t B;
+  int32_t max_pages;
+  int32_t page_size;          /* power of two, 8..4096 */
+  int32_t T;
+} smla_seqs_t;
+
+/* Stage 1 -- FP8 lightning-indexer scores.
+ * "sparse_index_fp8_sm100" (Modular Mojo kernel page), module summary and
+ * section "Layout (crux)":
+ *   scores[t, key] = k_scale[phys(key)] * sum_h relu(q[t,h,:] . k_pool[phys(key),:]) * q_scale[t,h]
+ * for every logical key 0..pos(t) of t's sequence; every other entry of row
+ * t (key > pos(t), up to score_stride) is written as -inf (the causal tail
+ * fill, fused).
+ *   q        e4m3 [T, H_idx, 128]
+ *   q_scale  f32  [T, H_idx]
+ *   k_pool   e4m3 [phys_rows, 128]  paged indexer keys
+ *   k_scale  f32  [phys_rows]       per physical row
+ *   scores   f32  [T, score_stride] (output; score_stride >= max kv_len, multiple of 4)
+ * H_idx must be 4, 8, 16, 32 or 64 (SMLA_ERR_UNSUPPORTED otherwise).
+ * The dot products run on tcgen05 FP8 tensor cores with f32 accumulation. */
+smla_status_t smla_indexer_scores(const uint8_t* q, const float* q_scale, const uint8_t* k_pool,
+                                  const float* k_scale, int64_t phys_rows, smla_seqs_t seqs,
+                                  int32_t H_idx, float* scores, int64_t score_stride,
+                                  cudaStream_t stream);
+
+/* Stage 2 -- per-token top-k over the causally valid keys.
+ * "sparse_index_fp8_sm100" (the score buffer "the top-k stage consumes",
+ * verified by a top-k set match) and "mla_sm100_prefill_sparse_fp8"
+ * (indices in physical-row space + per-query topk_lengths):
+ *   topk_lengths[t] = min(k, pos(t)+1)
+ *   indices[t, 0..len) = physical rows of the len largest scores[t, 0..pos(t)],
+ *                        ties broken toward the lower logical key, emitted in
+ *                        ascending logical-key order
+ *   indices[t, len..k) = 0xFFFFFFFF
+ *   scores   f32 [T, score_stride] (entries past pos(t) are not read)
+ *   indices  u32 [T, k] (output), topk_lengths u32 [T] (output)
+ * 1 <= k <= 65536. NaN scores are unsupported (their order is unspecified). */
+smla_status_t smla_topk(const float* scores, int64_t score_stride, smla_seqs_t seqs, int32_t k,
+                        uint32_t* indices, uint32_t* topk_lengths, cudaStream_t stream);
+
+/* Stage 3 -- sparse MLA prefill attention.
+ * "mla_sm100_prefill_sparse_fp8" (Modular Mojo function page: arguments,
+ * scale_block_size modes) and "mla_prefill_sparse_qkv_fp8" (K and V share
+ * the latent rows; V = the first v_depth columns).  For each token t and
+ * head h, with n = topk_lengths[t] and K_j = dequant(latent_pool[indices[t,j]]):
+ *   s_j = softmax_scale * q[t,h,:] . K_j,   p = softmax(s_0..s_{n-1}),
+ *   out[t,h,:] = bf16_rne( sum_j p_j * K_j[0:v_depth] )     (zeros if n == 0)
+ *   q            [T, H, 576], bf16 (q_dtype SMLA_BF16) or e4m3 (SMLA_E4M3)
+ *   latent_pool  e4m3 [phys_rows, 576] (512 nope + 64 rope)
+ *   scales       f32 [phys_rows, ceil(576/scale_block_size)]; NULL when
+ *                scale_block_size == 0 (unit scale); scale_block_size >= 576
+ *                means one scale per row; 32 means 18 block scales per row
+ *   indices      u32 [T, indices_stride] physical rows; topk_lengths u32 [T]
+ *                (each <= indices_stride)
+ *   out          bf16 [T, H, v_depth] (output)
+ * Supported: H in {16, 64, 128} (any multiple of 64, or 16..64 padded),
+ * v_depth == 512, scale_block_size in {0, 32} or >= 576; attn_sink must be
+ * NULL (the pages do not define its semantics).
+ * Runs on tcgen05 FP8 tensor cores with f32 TMEM accumulation: e4m3 q is
+ * used natively; bf16 q and the softmax weights P (bf16-accuracy path) are
+ * carried as two e4m3 terms (hi + lo) so that the products stay on the FP8
+ * pipe; blockwise-scaled rows are dequantised to the same two-term form. */
+smla_status_t smla_sparse_prefill(const void* q, int32_t q_dtype, const uint8_t* latent_pool,
+                                  int64_t phys_rows, const float* scales, int32_t scale_block_size,
+                                  const uint32_t* indices, int32_t indices_stride,
+                                  const uint32_t* topk_lengths, int32_t T, int32_t H,
+                                  int32_t v_depth, float softmax_scale, const float* attn_sink,
+                                  uint16_t* out, cudaStream_t stream);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns SMLA_OK, SMLA_ERR_DEVICE_CHECK (out-of-range index or page
+ * id), SMLA_ERR_TIMEOUT (a pipeline wait gave up) or SMLA_ERR_CUDA. */
+smla_status_t smla_check_device_errors(cudaStream_t stream);
+
+/* Copies the calling thread's last error message (NUL-terminated, truncated
+ * to n bytes) and returns its full length. */
+size_t smla_last_error(char* buf, size_t n);
+
+/* Library version, "major.minor.patch". */
+const char* smla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SMLA_H_ */

@@ -1,0 +1,18 @@
+"""GB300 (sm_103a) FP8 lightning indexer -> top-k -> sparse MLA prefill.
+
+The compute runs in libsmla.so (hand-written CUDA + inline PTX); this package
+holds its ctypes binding (``_lib``), the in-tree build (``build``) and the
+seeded synthetic input generators (``workloads``).  Importing the package
+does not load the library; the binding's first call does, and raises if the
+library is missing.
+"""
+from ._lib import (  # noqa: F401
+    Seqs,
+    SmlaError,
+    indexer_scores,
+    topk,
+    sparse_prefill,
+    check_device_errors,
+    version,
+    load,
+)

@@ -1,0 +1,222 @@
+// The C ABI (include/smla.h): host-side argument validation, the per-device
+// error word, tensor-map encoding and dispatch to the stage launchers.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "ptx.cuh"
+#include "smla_internal.h"
+
+namespace smla {
+
+namespace {
+thread_local std::string g_last_error;
+std::mutex g_mu;
+constexpr int kMaxDevices = 64;
+unsigned* g_err_ptr[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+}  // namespace
+
+// One word per device; kernels atomicOr error bits into it.
+__device__ unsigned int g_smla_device_errors;
+
+smla_status_t fail(smla_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+smla_status_t fail_cuda(cudaError_t e, const char* what) {
+  return fail(SMLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool encode_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                      uint32_t box_rows) {
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  // The driver entry point is looked up through the runtime, so the library
+  // does not link libcuda directly (it loads on machines without a driver).
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn encode = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return false;
+      encode = reinterpret_cast<EncodeFn>(fn);
+    }
+  }
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static smla_status_t device_err_ptr(unsigned** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(SMLA_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_smla_device_errors);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(device error word)");
+    g_err_ptr[dev] = static_cast<unsigned*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return SMLA_OK;
+}
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sm_count[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+static smla_status_t check_seqs(const smla_seqs_t& s) {
+  if (s.T < 0 || s.B < 0) return fail(SMLA_ERR_INVALID_ARG, "seqs: T=%d B=%d must be >= 0", s.T, s.B);
+  if (s.T == 0) return SMLA_OK;
+  if (s.B < 1) return fail(SMLA_ERR_INVALID_ARG, "seqs: B must be >= 1 when T > 0");
+  if (!s.cu_q || !s.kv_len || !s.page_table) return fail(SMLA_ERR_INVALID_ARG, "seqs: null pointer");
+  if (!aligned4(s.cu_q) || !aligned4(s.kv_len) || !aligned4(s.page_table))
+    return fail(SMLA_ERR_INVALID_ARG, "seqs: pointers must be 4-byte aligned");
+  if (s.max_pages < 1) return fail(SMLA_ERR_INVALID_ARG, "seqs: max_pages must be >= 1");
+  if (s.page_size < 8 || s.page_size > 4096 || (s.page_size & (s.page_size - 1)))
+    return fail(SMLA_ERR_UNSUPPORTED, "seqs: page_size %d must be a power of two in [8, 4096]", s.page_size);
+  return SMLA_OK;
+}
+
+}  // namespace smla
+
+using namespace smla;
+
+extern "C" {
+
+const char* smla_version(void) { return "0.1.0"; }
+
+size_t smla_last_error(char* buf, size_t n) {
+  const std::string& m = g_last_error;
+  if (buf && n) {
+    const size_t c = m.size() < n - 1 ? m.size() : n - 1;
+    std::memcpy(buf, m.data(), c);
+    buf[c] = '\0';
+  }
+  return m.size();
+}
+
+smla_status_t smla_indexer_scores(const uint8_t* q, const float* q_scale, const uint8_t* k_pool,
+                                  const float* k_scale, int64_t phys_rows, smla_seqs_t seqs, int32_t H_idx,
+                                  float* scores, int64_t score_stride, cudaStream_t stream) {
+  g_last_error.clear();
+  smla_status_t st = check_seqs(seqs);
+  if (st != SMLA_OK) return st;
+  if (H_idx != 4 && H_idx != 8 && H_idx != 16 && H_idx != 32 && H_idx != 64)
+    return fail(SMLA_ERR_UNSUPPORTED, "H_idx=%d: supported 4, 8, 16, 32, 64", H_idx);
+  if (score_stride < 4 || (score_stride & 3))
+    return fail(SMLA_ERR_INVALID_ARG, "score_stride=%lld must be a positive multiple of 4",
+                static_cast<long long>(score_stride));
+  if (seqs.T == 0) return SMLA_OK;
+  if (!q || !q_scale || !k_pool || !k_scale || !scores) return fail(SMLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(scores) || !aligned4(q_scale) || !aligned4(k_scale))
+    return fail(SMLA_ERR_INVALID_ARG, "q, k_pool, scores must be 16-byte aligned; scales 4-byte aligned");
+  if (phys_rows < 1 || phys_rows >= (int64_t(1) << 31))
+    return fail(SMLA_ERR_INVALID_ARG, "phys_rows=%lld out of range", static_cast<long long>(phys_rows));
+  if (static_cast<int64_t>(seqs.T) * H_idx >= (int64_t(1) << 31))
+    return fail(SMLA_ERR_UNSUPPORTED, "T*H_idx too large");
+  unsigned* err = nullptr;
+  st = device_err_ptr(&err);
+  if (st != SMLA_OK) return st;
+  return launch_indexer(q, q_scale, k_pool, k_scale, phys_rows, seqs, H_idx, scores, score_stride, err, stream);
+}
+
+smla_status_t smla_topk(const float* scores, int64_t score_stride, smla_seqs_t seqs, int32_t k, uint32_t* indices,
+                        uint32_t* topk_lengths, cudaStream_t stream) {
+  g_last_error.clear();
+  smla_status_t st = check_seqs(seqs);
+  if (st != SMLA_OK) return st;
+  if (k < 1 || k > 65536) return fail(SMLA_ERR_UNSUPPORTED, "k=%d must be in [1, 65536]", k);
+  if (score_stride < 4 || (score_stride & 3))
+    return fail(SMLA_ERR_INVALID_ARG, "score_stride=%lld must be a positive multiple of 4",
+                static_cast<long long>(score_stride));
+  if (seqs.T == 0) return SMLA_OK;
+  if (!scores || !indices || !topk_lengths) return fail(SMLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(scores) || !aligned4(indices) || !aligned4(topk_lengths))
+    return fail(SMLA_ERR_INVALID_ARG, "scores must be 16-byte aligned; outputs 4-byte aligned");
+  unsigned* err = nullptr;
+  st = device_err_ptr(&err);
+  if (st != SMLA_OK) return st;
+  return launch_topk(scores, score_stride, seqs, k, indices, topk_lengths, err, stream);
+}
+
+smla_status_t smla_sparse_prefill(const void* q, int32_t q_dtype, const uint8_t* latent_pool, int64_t phys_rows,
+                                  const float* scales, int32_t scale_block_size, const uint32_t* indices,
+                                  int32_t indices_stride, const uint32_t* topk_lengths, int32_t T, int32_t H,
+                                  int32_t v_depth, float softmax_scale, const float* attn_sink, uint16_t* out,
+                                  cudaStream_t stream) {
+  g_last_error.clear();
+  if (T < 0) return fail(SMLA_ERR_INVALID_ARG, "T=%d must be >= 0", T);
+  if (q_dtype != SMLA_BF16 && q_dtype != SMLA_E4M3) return fail(SMLA_ERR_INVALID_ARG, "q_dtype=%d", q_dtype);
+  if (!(H >= 1 && ((H <= 64 && H % 16 == 0) || H % 64 == 0)))
+    return fail(SMLA_ERR_UNSUPPORTED, "H=%d: supported 16, 32, 48, 64 or a multiple of 64", H);
+  if (v_depth != 512) return fail(SMLA_ERR_UNSUPPORTED, "v_depth=%d: only 512 is supported", v_depth);
+  if (!(scale_block_size == 0 || scale_block_size == 32 || scale_block_size >= 576))
+    return fail(SMLA_ERR_UNSUPPORTED, "scale_block_size=%d: supported 0, 32 or >= 576", scale_block_size);
+  if (scale_block_size != 0 && !scales) return fail(SMLA_ERR_INVALID_ARG, "scales is NULL with scale_block_size != 0");
+  if (attn_sink) return fail(SMLA_ERR_UNSUPPORTED, "attn_sink must be NULL");
+  if (!(softmax_scale == softmax_scale) || softmax_scale > 3.0e38f || softmax_scale < -3.0e38f)
+    return fail(SMLA_ERR_INVALID_ARG, "softmax_scale must be finite");
+  if (indices_stride < 1) return fail(SMLA_ERR_INVALID_ARG, "indices_stride must be >= 1");
+  if (T == 0) return SMLA_OK;
+  if (!q || !latent_pool || !indices || !topk_lengths || !out) return fail(SMLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(q) || !aligned16(latent_pool) || !aligned16(out) || !aligned4(indices) || !aligned4(topk_lengths) ||
+      (scales && !aligned4(scales)))
+    return fail(SMLA_ERR_INVALID_ARG, "q, latent_pool, out must be 16-byte aligned; indices/scales 4-byte aligned");
+  if (phys_rows < 1 || phys_rows >= (int64_t(1) << 31))
+    return fail(SMLA_ERR_INVALID_ARG, "phys_rows=%lld out of range", static_cast<long long>(phys_rows));
+  unsigned* err = nullptr;
+  smla_status_t st = device_err_ptr(&err);
+  if (st != SMLA_OK) return st;
+  return launch_sparse_prefill(q, q_dtype, latent_pool, phys_rows, scales, scale_block_size, indices,
+                               indices_stride, topk_lengths, T, H, softmax_scale, out, err, stream);
+}
+
+smla_status_t smla_check_device_errors(cudaStream_t stream) {
+  g_last_error.clear();
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+  unsigned v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_smla_device_errors, sizeof(v));
+  if (e != cudaSuccess) return fail_cuda(e, "read device error word");
+  if (v == 0) return SMLA_OK;
+  const unsigned zero = 0;
+  e = cudaMemcpyToSymbol(g_smla_device_errors, &zero, sizeof(zero));
+  if (e != cudaSuccess) return fail_cuda(e, "clear device error word");
+  if (v & kErrTimeout) return fail(SMLA_ERR_TIMEOUT, "device error word 0x%x: a pipeline wait gave up", v);
+  return fail(SMLA_ERR_DEVICE_CHECK, "device error word 0x%x: index/page/shape out of range", v);
+}
+
+}  // extern "C"

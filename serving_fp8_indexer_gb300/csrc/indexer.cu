@@ -1,0 +1,339 @@
+// Stage 1: FP8 lightning-indexer scores on tcgen05 tensor cores.
+//
+// "sparse_index_fp8_sm100" (Modular Mojo kernel page), module summary and
+// "Layout (crux)":
+//   score[t, key] = k_scale[key] * sum_h relu(q[t,h] . k[key]) * q_scale[t,h]
+// computed as S^T = K . Q^T with the key tile as the MMA M dimension, so the
+// head reduction of a key's row stays inside one thread after tcgen05.ld.
+//
+// GB300 design (not the page's SM100 one):
+//   * MMA 128 keys (M) x 256 (token, head) columns (N) x 128 depth (K),
+//     kind::f8f6f4 e4m3 x e4m3 -> f32 in TMEM; 4 instructions of K = 32.
+//     With H_idx = 64 one tile covers 4 tokens (256 / H_idx in general).
+//   * A work item is (sequence, token tile, key chunk).  Q and q_scale are
+//     loaded once per item; K tiles stream through a 4-stage TMA ring, one
+//     box per page (page_size >= 128: one box per tile), so the paged cache
+//     is read in place.  Key tiles wholly past the last token's position
+//     are not computed, only filled with -inf.
+//   * Two TMEM accumulators (2 x 256 columns) let the MMA of tile i+1 run
+//     while 8 epilogue warps drain tile i: relu, x q_scale, sum over the
+//     token's heads, x k_scale, causal -inf, coalesced f32 stores.
+//   * Warp roles: warp 0 TMA producer, warp 1 MMA issuer (and TMEM owner),
+//     warps 2..9 epilogue.
+#include <algorithm>
+
+#include "ptx.cuh"
+#include "smla_internal.h"
+
+namespace smla {
+namespace idx {
+
+constexpr int kDepth = 128;
+constexpr int kBM = 128;      // keys per tile (MMA M)
+constexpr int kBN = 256;      // (token, head) columns per tile (MMA N)
+constexpr int kStages = 4;
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;
+constexpr uint32_t kTmemCols = 512;
+
+struct Params {
+  const float* q_scale;
+  const float* k_scale;
+  int64_t phys_rows;
+  const int32_t* cu_q;
+  const int32_t* kv_len;
+  const int32_t* page_table;
+  int B, max_pages, page_size, T;
+  float* scores;
+  int64_t score_stride;
+  int chunk_tiles;  // key tiles per work item
+  int box_rows;     // rows per K TMA box = min(page_size, 128)
+  unsigned* err;
+};
+
+struct __align__(1024) Smem {
+  uint8_t q[kBN * kDepth];            // SW128 K-major: 256 rows x 128 B
+  uint8_t k[kStages][kBM * kDepth];   // SW128 K-major: 128 rows x 128 B each
+  float qs[kBN];
+  unsigned long long bar_q, bar_kfull[kStages], bar_kempty[kStages], bar_afull[2], bar_aempty[2], bar_drain;
+  uint32_t tmem_base;
+  int item_b, item_tt, item_kc;
+};
+
+template <int HIDX>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const Params p) {
+  constexpr int TOK = kBN / HIDX;      // tokens per tile
+  constexpr int HALF_TOK = TOK / 2;    // tokens per epilogue column half
+  constexpr uint32_t IDESC = idesc_e4m3_f32(kBM, kBN, 0, 0);
+
+  extern __shared__ uint8_t smem_raw[];
+  Smem& s = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int CW = p.chunk_tiles * kBM;
+
+  // ---- resolve this CTA's work item (warp 0 scans the sequences)
+  if (warp == 0) {
+    int base = 0, found_b = -1, found_tt = 0, found_kc = 0;
+    const int target = blockIdx.x;
+    for (int b0 = 0; b0 < p.B && found_b < 0; b0 += 32) {
+      const int b = b0 + lane;
+      int n = 0, ntt = 0, nkc = 0;
+      if (b < p.B) {
+        const int ql = p.cu_q[b + 1] - p.cu_q[b];
+        const int kl = p.kv_len[b];
+        ntt = (ql + TOK - 1) / TOK;
+        nkc = (kl + CW - 1) / CW;
+        n = (ql > 0 && kl >= ql && kl <= p.score_stride) ? ntt * nkc : 0;
+        if (ql > 0 && (kl < ql || kl > p.score_stride)) atomicOr(p.err, kErrShape);
+      }
+      int incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const int excl = base + incl - n;
+      const bool mine = n > 0 && target >= excl && target < excl + n;
+      const unsigned ball = __ballot_sync(0xffffffffu, mine);
+      if (ball) {
+        const int src = __ffs(ball) - 1;
+        if (lane == src) {
+          const int r = target - excl;
+          found_b = b;
+          found_tt = r / nkc;
+          found_kc = r % nkc;
+        }
+        found_b = __shfl_sync(0xffffffffu, found_b, src);
+        found_tt = __shfl_sync(0xffffffffu, found_tt, src);
+        found_kc = __shfl_sync(0xffffffffu, found_kc, src);
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      s.item_b = found_b;
+      s.item_tt = found_tt;
+      s.item_kc = found_kc;
+    }
+  }
+  __syncthreads();
+  if (s.item_b < 0) return;
+
+  const int b = s.item_b, tt = s.item_tt, kc = s.item_kc;
+  const int cu0 = p.cu_q[b];
+  const int q_len = p.cu_q[b + 1] - cu0;
+  const int kvl = p.kv_len[b];
+  const int t0 = cu0 + tt * TOK;
+  const int ntok = min(TOK, q_len - tt * TOK);
+  const int pos0 = kvl - q_len + tt * TOK;
+  const int key_lo = kc * CW;
+  const int key_hi = min(key_lo + CW, kvl);
+  const int64_t cover_hi = (key_hi == kvl) ? p.score_stride : key_hi;  // last chunk also fills past kv_len
+  const int max_pos = pos0 + ntok - 1;
+  const int kt_begin = key_lo / kBM;
+  const int kt_end = min((key_hi + kBM - 1) / kBM, max_pos / kBM + 1);
+  const int n_tiles = max(0, kt_end - kt_begin);
+
+  // ---- setup: barriers, TMEM, q_scale tile
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&s.bar_q), 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(smem_u32(&s.bar_kfull[i]), 1);
+      mbar_init(smem_u32(&s.bar_kempty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s.bar_afull[i]), 1);
+      mbar_init(smem_u32(&s.bar_aempty[i]), kEpiThreads);
+    }
+    mbar_init(smem_u32(&s.bar_drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&s.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp >= 2) {
+    const int c = threadIdx.x - 64;  // 0..255 = column (token-in-tile, head)
+    const int tok = c / HIDX, h = c % HIDX;
+    s.qs[c] = (tok < ntok) ? p.q_scale[static_cast<int64_t>(t0 + tok) * HIDX + h] : 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0 && n_tiles > 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      mbar_arrive_expect_tx(smem_u32(&s.bar_q), kBN * kDepth);
+      tma_load_2d(smem_u32(s.q), &tm_q, 0, t0 * HIDX, smem_u32(&s.bar_q));
+      const int nbox = kBM / p.box_rows;
+      for (int i = 0; i < n_tiles; ++i) {
+        const int st = i % kStages;
+        if (!mbar_wait(smem_u32(&s.bar_kempty[st]), ((i / kStages) & 1) ^ 1, p.err)) break;
+        const int kt = kt_begin + i;
+        int nload = 0;
+        int rows[kBM / 8];
+        for (int bx = 0; bx < nbox; ++bx) {
+          const int key0 = kt * kBM + bx * p.box_rows;
+          rows[bx] = -1;
+          if (key0 >= kvl) continue;
+          const int page = key0 / p.page_size;
+          const int pid = page < p.max_pages ? p.page_table[static_cast<int64_t>(b) * p.max_pages + page] : -1;
+          const int64_t row = static_cast<int64_t>(pid) * p.page_size + key0 % p.page_size;
+          if (pid < 0 || row + p.box_rows > p.phys_rows) {
+            atomicOr(p.err, kErrPage);
+            continue;
+          }
+          rows[bx] = static_cast<int>(row);
+          ++nload;
+        }
+        // A tile whose boxes were all rejected still arrives (with no bytes).
+        mbar_arrive_expect_tx(smem_u32(&s.bar_kfull[st]), nload * p.box_rows * kDepth);
+        for (int bx = 0; bx < nbox; ++bx)
+          if (rows[bx] >= 0)
+            tma_load_2d(smem_u32(s.k[st]) + bx * p.box_rows * kDepth, &tm_k, 0, rows[bx],
+                        smem_u32(&s.bar_kfull[st]));
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      bool ok = mbar_wait(smem_u32(&s.bar_q), 0, p.err);
+      const uint32_t q_base = smem_u32(s.q);
+      for (int i = 0; ok && i < n_tiles; ++i) {
+        const int st = i % kStages, a = i & 1;
+        if (!mbar_wait(smem_u32(&s.bar_kfull[st]), (i / kStages) & 1, p.err)) break;
+        if (!mbar_wait(smem_u32(&s.bar_aempty[a]), ((i >> 1) & 1) ^ 1, p.err)) break;
+        tc_fence_after();
+        const uint32_t k_base = smem_u32(s.k[st]);
+#pragma unroll
+        for (int kk = 0; kk < kDepth / 32; ++kk) {
+          const uint64_t ad = make_sdesc(k_base + kk * 32, 16, 1024, kSwizzle128B);
+          const uint64_t bd = make_sdesc(q_base + kk * 32, 16, 1024, kSwizzle128B);
+          mma_f8f6f4_ss(tmem + a * kBN, ad, bd, IDESC, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&s.bar_kempty[st]));
+        mma_commit(smem_u32(&s.bar_afull[a]));
+      }
+      // Make sure no MMA is still writing TMEM when the CTA tears down.
+      mma_commit(smem_u32(&s.bar_drain));
+      mbar_wait(smem_u32(&s.bar_drain), 0, p.err);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int ew = warp - 2;           // 0..7
+    const int quarter = warp & 3;      // TMEM lanes this warp may access
+    const int half = ew >> 2;          // column half: tokens [half*HALF_TOK, +HALF_TOK)
+    const int row = quarter * 32 + lane;
+    const float* qs = s.qs + half * (kBN / 2);
+    for (int i = 0; i < n_tiles; ++i) {
+      const int a = i & 1;
+      const int kt = kt_begin + i;
+      const int key = kt * kBM + row;
+      // k_scale of this lane's key (physical row) while the MMA runs.
+      float ks = 0.f;
+      if (key < kvl) {
+        const int page = key / p.page_size;
+        const int pid = page < p.max_pages ? p.page_table[static_cast<int64_t>(b) * p.max_pages + page] : -1;
+        const int64_t prow = static_cast<int64_t>(pid) * p.page_size + key % p.page_size;
+        if (pid >= 0 && prow < p.phys_rows) ks = p.k_scale[prow];
+      }
+      if (!mbar_wait(smem_u32(&s.bar_afull[a]), (i >> 1) & 1, p.err)) break;
+      tc_fence_after();
+      float acc[HALF_TOK];
+#pragma unroll
+      for (int j = 0; j < HALF_TOK; ++j) acc[j] = 0.f;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * kBN + half * (kBN / 2);
+#pragma unroll
+      for (int cb = 0; cb < kBN / 2; cb += 32) {
+        uint32_t v[32];
+        tmem_ld32(taddr + cb, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float x = fmaxf(__uint_as_float(v[j]), 0.f);
+          acc[(cb + j) / HIDX] = fmaf(x, qs[cb + j], acc[(cb + j) / HIDX]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&s.bar_aempty[a]));
+      if (key >= key_lo && key < cover_hi) {
+#pragma unroll
+        for (int j = 0; j < HALF_TOK; ++j) {
+          const int tok = half * HALF_TOK + j;
+          if (tok < ntok) {
+            const float v = (key <= pos0 + tok) ? ks * acc[j] : -INFINITY;
+            p.scores[static_cast<int64_t>(t0 + tok) * p.score_stride + key] = v;
+          }
+        }
+      }
+    }
+    // -inf for the covered keys no computed tile reached.
+    const int64_t fill_lo = max(static_cast<int64_t>(key_lo), static_cast<int64_t>(kt_end) * kBM);
+    const int et = threadIdx.x - 64;
+    for (int tok = 0; tok < ntok; ++tok) {
+      float* dst = p.scores + static_cast<int64_t>(t0 + tok) * p.score_stride;
+      for (int64_t key = fill_lo + et; key < cover_hi; key += kEpiThreads) dst[key] = -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int HIDX>
+static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const Params& p, int grid,
+                            cudaStream_t stream) {
+  const size_t smem = sizeof(Smem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(indexer_kernel<HIDX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  indexer_kernel<HIDX><<<grid, kThreads, smem, stream>>>(tq, tk, p);
+  return cudaGetLastError();
+}
+
+}  // namespace idx
+
+// Host launcher: builds the two tensor maps, sizes the work items and launches.
+smla_status_t launch_indexer(const uint8_t* q, const float* q_scale, const uint8_t* k_pool, const float* k_scale,
+                             int64_t phys_rows, const smla_seqs_t& seqs, int h_idx, float* scores,
+                             int64_t score_stride, unsigned* err, cudaStream_t stream) {
+  using namespace idx;
+  if (seqs.T == 0 || seqs.B == 0) return SMLA_OK;
+  const int tok = kBN / h_idx;
+  const int box_rows = std::min(seqs.page_size, kBM);
+  CUtensorMap tq, tk;
+  if (!encode_tma_2d_u8(&tq, q, kDepth, static_cast<uint64_t>(seqs.T) * h_idx, kDepth, kBN))
+    return fail(SMLA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the indexer Q tensor map");
+  if (!encode_tma_2d_u8(&tk, k_pool, kDepth, static_cast<uint64_t>(phys_rows), kDepth, box_rows))
+    return fail(SMLA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the indexer K tensor map");
+  // Key chunk per work item: enough items to give every SM about two.
+  const int64_t key_tiles = (score_stride + kBM - 1) / kBM;
+  const int64_t est_tt = (seqs.T + tok - 1) / tok;
+  int64_t chunk = (est_tt * key_tiles + 2 * 152 - 1) / (2 * 152);
+  chunk = std::max<int64_t>(1, std::min<int64_t>(chunk, key_tiles));
+  const int64_t nchunk = (key_tiles + chunk - 1) / chunk;
+  const int64_t grid = (est_tt + seqs.B) * nchunk;  // upper bound; CTAs past the last item exit at once
+  if (grid > 0x7fffffff) return fail(SMLA_ERR_UNSUPPORTED, "indexer grid too large");
+  Params p{q_scale, k_scale, phys_rows, seqs.cu_q, seqs.kv_len, seqs.page_table, seqs.B, seqs.max_pages,
+           seqs.page_size, seqs.T, scores, score_stride, static_cast<int>(chunk), box_rows, err};
+  cudaError_t e;
+  switch (h_idx) {
+    case 4: e = launch_t<4>(tq, tk, p, static_cast<int>(grid), stream); break;
+    case 8: e = launch_t<8>(tq, tk, p, static_cast<int>(grid), stream); break;
+    case 16: e = launch_t<16>(tq, tk, p, static_cast<int>(grid), stream); break;
+    case 32: e = launch_t<32>(tq, tk, p, static_cast<int>(grid), stream); break;
+    case 64: e = launch_t<64>(tq, tk, p, static_cast<int>(grid), stream); break;
+    default: return fail(SMLA_ERR_UNSUPPORTED, "H_idx must be 4, 8, 16, 32 or 64");
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "indexer launch");
+  return SMLA_OK;
+}
+
+}  // namespace smla

@@ -1,0 +1,36 @@
+// Host-side internals shared by the library's translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/smla.h"
+
+namespace smla {
+
+// Records a message for smla_last_error() and returns `st`.
+smla_status_t fail(smla_status_t st, const char* fmt, ...);
+smla_status_t fail_cuda(cudaError_t e, const char* what);
+
+// 2-D uint8 tensor map [rows][inner] (row pitch = inner bytes), box
+// [box_rows][box_inner], 128-byte swizzle, zero fill out of bounds.
+bool encode_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                      uint32_t box_rows);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+smla_status_t launch_indexer(const uint8_t* q, const float* q_scale, const uint8_t* k_pool, const float* k_scale,
+                             int64_t phys_rows, const smla_seqs_t& seqs, int h_idx, float* scores,
+                             int64_t score_stride, unsigned* err, cudaStream_t stream);
+
+smla_status_t launch_topk(const float* scores, int64_t score_stride, const smla_seqs_t& seqs, int k,
+                          uint32_t* indices, uint32_t* topk_lengths, unsigned* err, cudaStream_t stream);
+
+smla_status_t launch_sparse_prefill(const void* q, int q_dtype, const uint8_t* latent, int64_t phys_rows,
+                                    const float* scales, int sbs, const uint32_t* indices, int indices_stride,
+                                    const uint32_t* topk_lengths, int T, int H, float softmax_scale,
+                                    uint16_t* out, unsigned* err, cudaStream_t stream);
+
+}  // namespace smla
