@@ -242,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t prow = static_cast<int64_t>(pid) * p.page_size + key % p.page_size;
         if (pid >= 0 && prow < p.phys_rows) ks = p.k_scale[prow];
       }
-      if (!mbar_wait(smem_u32(&s.bar_afull[a]), (i >> 1) & 1, p.err)) break;
+      // warp-uniform: the tcgen05.ld below is warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_afull[a]), (i >> 1) & 1, p.err))) break;
       tc_fence_after();
       float acc[HALF_TOK];
 #pragma unroll

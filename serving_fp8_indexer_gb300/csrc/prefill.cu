@@ -1,7 +1,536 @@
+// Stage 3: sparse MLA prefill attention on tcgen05 FP8 tensor cores.
+//
+// What it computes ("mla_sm100_prefill_sparse_fp8" function page; K and V
+// share the latent rows per "mla_prefill_sparse_qkv_fp8"): for token t,
+// head h and the n = topk_lengths[t] gathered latent rows K_j,
+//   out[t,h,:] = sum_j softmax_j(softmax_scale * q[t,h] . K_j) * K_j[0:512].
+//
+// GB300 design.  One CTA per (token, group of 64 heads); the token's keys
+// are processed in blocks of 128 gathered rows.  The block's keys are the
+// MMA M dimension and the heads the N dimension:
+//   S^T[128 keys x 64 heads] = K_blk . Q^T           (TMEM, 64 columns)
+//   O^T[512 vcols x 64 heads] += V_blk^T . P^T       (TMEM, 4 x 64 columns)
+// so the 128-head, 512-wide output of a token never has to sit in TMEM at
+// once (a [heads x 512] f32 accumulator alone would fill all 512 columns)
+// and every MMA is M = 128 at full rate.  V^T is the same gathered buffer
+// read MN-major (V = the first 512 columns of K).
+//
+// All products run on the FP8 pipe (kind::f8f6f4, f32 accumulation):
+//   * e4m3 q is used as is; bf16 q is split once per CTA into two e4m3
+//     terms q*2^e = hi + lo (per-head power-of-two 2^e keeps lo in range),
+//     both multiplied into the same S accumulator (error ~2^-8 relative);
+//   * P is quantised to one e4m3 term (native FP8-P path) or, for the bf16
+//     path, to hi + lo like q;
+//   * blockwise-scaled rows (32-wide scales) are dequantised in registers
+//     during the gather to x * s_blk / s_row and stored as e4m3 hi + lo,
+//     after which every row carries one scale s_row.
+// A per-row scale s_j (tensorwise, or s_row) enters exactly: the logit is
+// z = acc * s_j * c_h, the PV operand is exp2(z + log2 s_j - m) and the
+// normaliser sums exp2(z - m), so out = sum_j p_j s_j Vraw_j / sum_j p_j.
+//
+// Softmax: keys are TMEM lanes, so a head's maximum is a cross-lane
+// reduction (warp redux on order-preserving ints, then across 4 warps).
+// The reference maximum m is only raised when a block exceeds it by more
+// than 2^8 (lazy rescale), keeping P <= 256 inside the e4m3 range; raising
+// it rescales O^T and the row sums.
+//
+// Warp roles: warps 0-3 softmax / epilogue (thread = key lane), warp 4
+// MMA issuer and TMEM owner, warps 5-7 gather producers.
+#include <algorithm>
+
+#include "ptx.cuh"
 #include "smla_internal.h"
+
 namespace smla {
-smla_status_t launch_sparse_prefill(const void*, int, const uint8_t*, int64_t, const float*, int, const uint32_t*, int,
-                                    const uint32_t*, int, int, float, uint16_t*, unsigned*, cudaStream_t) {
-  return fail(SMLA_ERR_UNSUPPORTED, "sparse prefill not built yet");
+namespace pf {
+
+constexpr int kD = 576;          // qk depth
+constexpr int kDV = 512;         // v depth
+constexpr int kNH = 64;          // heads per CTA (MMA N)
+constexpr int kBK = 128;         // keys per block (MMA M of QK)
+constexpr int kChunks = kD / 64; // 64-byte K chunks per row (SW64)
+constexpr int kQBytes = kChunks * kNH * 64;     // 36864
+constexpr int kKVBytes = kChunks * kBK * 64;    // 73728
+constexpr int kPBytes = kBK * kNH;              // 8192
+constexpr int kThreads = 256;
+constexpr int kSoftThreads = 128;
+constexpr int kProdThreads = 96;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 256;  // S^T columns [256, 320); O^T tiles at [0, 256)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kTau = 8.0f;      // lazy-rescale threshold (log2 units)
+
+enum Scale { kUnit = 0, kRow = 1, kBlock = 2 };
+
+struct Params {
+  const void* q;
+  const uint8_t* latent;
+  int64_t phys_rows;
+  const float* scales;
+  int nscale;  // scales per row
+  const uint32_t* indices;
+  int indices_stride;
+  const uint32_t* lens;
+  int T, H;
+  float softmax_scale;
+  uint16_t* out;
+  unsigned* err;
+};
+
+template <int QP, int KVP, int PP>
+struct Smem {
+  uint8_t q[QP][kQBytes];
+  uint8_t kv[KVP][kKVBytes];
+  uint8_t p[PP][kPBytes];
+  uint32_t idx[kBK];
+  float srow[kBK];       // per-row scale (1 for unit)
+  float lgrow[kBK];      // log2 of it
+  float cs[kNH];         // softmax_scale * log2(e) / 2^e_h
+  float mref[kNH];       // reference maximum per head (log2 units)
+  float fac[kNH];        // rescale factor of the current block
+  float red[4][kNH];     // cross-warp scratch
+  float linv[kNH];
+  int rescale;
+  unsigned long long bar_q, bar_kv_full, bar_kv_empty, bar_s_full, bar_p_full;
+  uint32_t tmem_base;
+};
+
+__device__ __forceinline__ int ord_int(float f) {
+  const int b = __float_as_int(f);
+  return b >= 0 ? b : b ^ 0x7fffffff;
 }
+__device__ __forceinline__ float ord_float(int o) { return __int_as_float(o >= 0 ? o : o ^ 0x7fffffff); }
+
+__device__ __forceinline__ uint32_t sw64(int row, int c4) { return static_cast<uint32_t>((c4 ^ ((row >> 1) & 3)) << 4); }
+
+// e4m3 hi + lo split of 16 floats into two 16-byte chunks.
+__device__ __forceinline__ void split16(const float (&x)[16], uint4& hi, uint4& lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint16_t h0 = f32x2_to_e4m3x2(x[4 * i + 0], x[4 * i + 1]);
+    const uint16_t h1 = f32x2_to_e4m3x2(x[4 * i + 2], x[4 * i + 3]);
+    const float2 b0 = e4m3x2_to_f32x2(h0), b1 = e4m3x2_to_f32x2(h1);
+    const uint16_t l0 = f32x2_to_e4m3x2(x[4 * i + 0] - b0.x, x[4 * i + 1] - b0.y);
+    const uint16_t l1 = f32x2_to_e4m3x2(x[4 * i + 2] - b1.x, x[4 * i + 3] - b1.y);
+    h[i] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
+    l[i] = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
+
+template <int QP, int KVP, int PP, int SC>
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
+  using S = Smem<QP, KVP, PP>;
+  extern __shared__ uint8_t smem_raw[];
+  S& s = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x;
+  const int g = blockIdx.y;
+  const int h0 = g * kNH;
+  const int hv = min(kNH, p.H - h0);  // valid heads of this CTA
+  int n = static_cast<int>(p.lens[t]);
+  if (n > p.indices_stride) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrShape);
+    n = p.indices_stride;
+  }
+  const int nblk = (n + kBK - 1) / kBK;
+  const uint32_t* tok_idx = p.indices + static_cast<int64_t>(t) * p.indices_stride;
+  uint16_t* out_t = p.out + (static_cast<int64_t>(t) * p.H + h0) * kDV;
+
+  if (n == 0) {  // empty selection: zeros (no softmax mass)
+    for (int i = threadIdx.x; i < hv * kDV / 8; i += kThreads) reinterpret_cast<uint4*>(out_t)[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&s.bar_q), kSoftThreads);
+    mbar_init(smem_u32(&s.bar_kv_full), kProdThreads);
+    mbar_init(smem_u32(&s.bar_kv_empty), 1);
+    mbar_init(smem_u32(&s.bar_s_full), 1);
+    mbar_init(smem_u32(&s.bar_p_full), kSoftThreads);
+    s.rescale = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(smem_u32(&s.tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+
+  if (warp < 4) {
+    // =================================================================== softmax / epilogue
+    const int r = threadIdx.x;  // key lane 0..127
+    // ---- Q: 2 threads per head, 288 elements each, as 18 groups of 16
+    {
+      const int hh = r >> 1, half = r & 1;
+      const bool hvalid = hh < hv;
+      float sigma = 1.f;
+      if (QP == 2) {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
+                                                          (static_cast<int64_t>(t) * p.H + h0 + hh) * kD + half * 288);
+        float amax = 0.f;
+        if (hvalid)
+          for (int i = 0; i < 36; ++i) {
+            const uint4 v = __ldg(src + i);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              amax = fmaxf(amax, fabsf(__uint_as_float(w[k] << 16)));
+              amax = fmaxf(amax, fabsf(__uint_as_float(w[k] & 0xffff0000u)));
+            }
+          }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        // scale so that the largest |q| * 2^e lies in [128, 256)
+        int e = 0;
+        if (amax > 0.f) {
+          int ex;
+          frexpf(amax, &ex);  // amax = m * 2^ex, m in [0.5, 1)
+          e = 8 - ex;
+        }
+        sigma = ldexpf(1.f, e);
+        for (int i = 0; i < 18; ++i) {
+          float x[16];
+          if (hvalid) {
+            const uint4 a = __ldg(src + 2 * i), b = __ldg(src + 2 * i + 1);
+            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              x[2 * k] = __uint_as_float(w[k] << 16) * sigma;
+              x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u) * sigma;
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) x[k] = 0.f;
+          }
+          uint4 hi, lo;
+          split16(x, hi, lo);
+          const int e0 = half * 288 + 16 * i;
+          const int kc = e0 >> 6, c4 = (e0 & 63) >> 4;
+          const uint32_t off = kc * (kNH * 64) + hh * 64 + sw64(hh, c4);
+          *reinterpret_cast<uint4*>(&s.q[0][off]) = hi;
+          *reinterpret_cast<uint4*>(&s.q[1 % QP][off]) = lo;
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) +
+                                                          (static_cast<int64_t>(t) * p.H + h0 + hh) * kD + half * 288);
+        for (int i = 0; i < 18; ++i) {
+          const uint4 v = hvalid ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+          const int e0 = half * 288 + 16 * i;
+          const int kc = e0 >> 6, c4 = (e0 & 63) >> 4;
+          *reinterpret_cast<uint4*>(&s.q[0][kc * (kNH * 64) + hh * 64 + sw64(hh, c4)]) = v;
+        }
+      }
+      if (half == 0) {
+        s.cs[hh] = p.softmax_scale * kLog2e / sigma;
+        s.mref[hh] = -INFINITY;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&s.bar_q));
+    }
+    named_bar_sync(1, kSoftThreads);
+
+    float lpart[kNH];
+#pragma unroll
+    for (int h = 0; h < kNH; ++h) lpart[h] = 0.f;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    bool ok = true;
+
+    for (int j = 0; ok && j < nblk; ++j) {
+      // S^T of block j is ready; kv_full is also waited so that the
+      // producers' per-row scales are visible to this thread.
+      bool w = mbar_wait(smem_u32(&s.bar_s_full), j & 1, p.err) &&
+               mbar_wait(smem_u32(&s.bar_kv_full), j & 1, p.err);
+      if (!named_bar_and(1, kSoftThreads, w)) { ok = false; break; }
+      tc_fence_after();
+      float z[kNH];
+      {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kTmemS, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 32; ++h) z[h] = __uint_as_float(v[h]);
+        tmem_ld32(tmem + lane_base + kTmemS + 32, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 32; ++h) z[32 + h] = __uint_as_float(v[h]);
+      }
+      tc_fence_before();
+      const bool valid = j * kBK + r < n;
+      const float sr = s.srow[r];
+      const float lg = s.lgrow[r];
+      // z = logit in log2 units; w = z + log2(s_row) is the PV operand's exponent
+      int mine0 = 0, mine1 = 0;
+#pragma unroll
+      for (int h = 0; h < kNH; ++h) {
+        z[h] = valid ? z[h] * sr * s.cs[h] : -INFINITY;
+        const int m = __reduce_max_sync(0xffffffffu, ord_int(z[h] + lg));
+        if (h < 32) { if (lane == h) mine0 = m; } else { if (lane == h - 32) mine1 = m; }
+      }
+      s.red[warp][lane] = ord_float(mine0);
+      s.red[warp][32 + lane] = ord_float(mine1);
+      named_bar_sync(1, kSoftThreads);
+      if (r < kNH) {
+        const float mb = fmaxf(fmaxf(s.red[0][r], s.red[1][r]), fmaxf(s.red[2][r], s.red[3][r]));
+        const float old = s.mref[r];
+        float f = 1.f;
+        if (mb > old + kTau) {
+          s.mref[r] = mb;
+          f = exp2f(old - mb);  // 0 when old is -inf
+          if (j > 0) s.rescale = 1;
+        }
+        s.fac[r] = f;
+      }
+      named_bar_sync(1, kSoftThreads);
+      const bool rescale = s.rescale != 0;
+      if (rescale) {
+        // O^T holds blocks < j: wait for the last PV, then scale each head's column.
+        w = mbar_wait(smem_u32(&s.bar_kv_empty), (j - 1) & 1, p.err);
+        if (!named_bar_and(1, kSoftThreads, w)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int tile = 0; tile < 4; ++tile) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t v[32];
+            const uint32_t a = tmem + lane_base + tile * kNH + c * 32;
+            tmem_ld32(a, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * s.fac[c * 32 + h]);
+            tmem_st32(a, v);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+      }
+#pragma unroll
+      for (int h = 0; h < kNH; ++h) lpart[h] *= s.fac[h];
+      named_bar_sync(1, kSoftThreads);
+      if (r == 0) s.rescale = 0;
+      // ---- P (row r of the [key][head] buffers), row sums
+      const float isr = 1.f / sr;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float x[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int h = c4 * 16 + k;
+          const float pw = exp2f(z[h] + lg - s.mref[h]);   // 0 for invalid rows
+          x[k] = pw;
+          lpart[h] += pw * isr;
+        }
+        if (PP == 2) {
+          uint4 hi, lo;
+          split16(x, hi, lo);
+          *reinterpret_cast<uint4*>(&s.p[0][r * 64 + sw64(r, c4)]) = hi;
+          *reinterpret_cast<uint4*>(&s.p[PP - 1][r * 64 + sw64(r, c4)]) = lo;
+        } else {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            w[i] = static_cast<uint32_t>(f32x2_to_e4m3x2(x[4 * i], x[4 * i + 1])) |
+                   (static_cast<uint32_t>(f32x2_to_e4m3x2(x[4 * i + 2], x[4 * i + 3])) << 16);
+          *reinterpret_cast<uint4*>(&s.p[0][r * 64 + sw64(r, c4)]) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&s.bar_p_full));
+    }
+
+    // ---- row sums across the 128 key lanes, then O^T / l -> bf16
+#pragma unroll
+    for (int h = 0; h < kNH; ++h) {
+      float v = lpart[h];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      lpart[h] = v;
+    }
+    if (lane == 0)
+#pragma unroll
+      for (int h = 0; h < kNH; ++h) s.red[warp][h] = lpart[h];
+    named_bar_sync(1, kSoftThreads);
+    if (r < kNH) {
+      const float l = s.red[0][r] + s.red[1][r] + s.red[2][r] + s.red[3][r];
+      s.linv[r] = l > 0.f ? 1.f / l : 0.f;
+    }
+    named_bar_sync(1, kSoftThreads);
+    const bool done = named_bar_and(1, kSoftThreads, ok && mbar_wait(smem_u32(&s.bar_kv_empty), (nblk - 1) & 1, p.err));
+    if (done) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int tile = 0; tile < 4; ++tile) {
+        const int vcol = tile * 128 + r;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + tile * kNH + c * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 32; ++h) {
+            const int hh = c * 32 + h;
+            if (hh < hv) {
+              const float o = __uint_as_float(v[h]) * s.linv[hh];
+              out_t[static_cast<int64_t>(hh) * kDV + vcol] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 4) {
+    // =================================================================== MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = idesc_e4m3_f32(kBK, kNH, 0, 0);
+      constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, kNH, 1, 1);
+      bool ok = mbar_wait(smem_u32(&s.bar_q), 0, p.err);
+      for (int j = 0; ok && j < nblk; ++j) {
+        if (!mbar_wait(smem_u32(&s.bar_kv_full), j & 1, p.err)) break;
+        tc_fence_after();
+        uint32_t acc = 0;
+#pragma unroll 1
+        for (int qp = 0; qp < QP; ++qp)
+#pragma unroll 1
+          for (int kp = 0; kp < KVP; ++kp)
+#pragma unroll
+            for (int kc = 0; kc < kChunks; ++kc)
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk) {
+                const uint64_t ad = make_sdesc(smem_u32(s.kv[kp]) + kc * (kBK * 64) + kk * 32, 16, 512, kSwizzle64B);
+                const uint64_t bd = make_sdesc(smem_u32(s.q[qp]) + kc * (kNH * 64) + kk * 32, 16, 512, kSwizzle64B);
+                mma_f8f6f4_ss(tmem + kTmemS, ad, bd, IDESC_QK, acc);
+                acc = 1;
+              }
+        mma_commit(smem_u32(&s.bar_s_full));
+        if (!mbar_wait(smem_u32(&s.bar_p_full), j & 1, p.err)) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int tile = 0; tile < 4; ++tile) {
+          uint32_t pacc = j > 0 ? 1u : 0u;
+#pragma unroll 1
+          for (int pp = 0; pp < PP; ++pp)
+#pragma unroll 1
+            for (int kp = 0; kp < KVP; ++kp)
+#pragma unroll
+              for (int ks = 0; ks < kBK / 32; ++ks) {
+                const uint64_t ad =
+                    make_sdesc(smem_u32(s.kv[kp]) + (2 * tile) * (kBK * 64) + ks * 32 * 64, kBK * 64, 512, kSwizzle64B);
+                const uint64_t bd = make_sdesc(smem_u32(s.p[pp]) + ks * 32 * 64, kBK * 64, 512, kSwizzle64B);
+                mma_f8f6f4_ss(tmem + tile * kNH, ad, bd, IDESC_PV, pacc);
+                pacc = 1;
+              }
+        }
+        mma_commit(smem_u32(&s.bar_kv_empty));
+      }
+    }
+  } else {
+    // =================================================================== gather producers
+    const int pt = threadIdx.x - 160;  // 0..95
+    const uint32_t first = tok_idx[0];
+    for (int j = 0; j < nblk; ++j) {
+      const bool w = mbar_wait(smem_u32(&s.bar_kv_empty), (j & 1) ^ 1, p.err);
+      if (!named_bar_and(2, kProdThreads, w)) break;
+      // rows pt, pt+96 of this block: physical row and scale
+      for (int rr = pt; rr < kBK; rr += kProdThreads) {
+        const int key = j * kBK + rr;
+        uint32_t row = key < n ? tok_idx[key] : first;
+        if (row >= static_cast<uint64_t>(p.phys_rows)) {
+          atomicOr(p.err, kErrIndex);
+          row = 0;
+        }
+        s.idx[rr] = row;
+        float sr = 1.f;
+        if (SC == kRow) {
+          sr = p.scales[static_cast<int64_t>(row) * p.nscale];
+        } else if (SC == kBlock) {
+          const float* sp = p.scales + static_cast<int64_t>(row) * p.nscale;
+          sr = 0.f;
+          for (int b = 0; b < p.nscale; ++b) sr = fmaxf(sr, sp[b]);
+          if (!(sr > 0.f)) sr = 1.f;
+        }
+        s.srow[rr] = sr;
+        s.lgrow[rr] = SC == kUnit ? 0.f : log2f(sr);
+      }
+      named_bar_sync(2, kProdThreads);
+      if (KVP == 1) {
+#pragma unroll 4
+        for (int it = 0; it < kBK * 36 / kProdThreads; ++it) {
+          const int i = it * kProdThreads + pt;
+          const int row = i / 36, c = i - row * 36;
+          const int kc = c >> 2, c4 = c & 3;
+          const uint32_t dst = smem_u32(s.kv[0]) + kc * (kBK * 64) + row * 64 + sw64(row, c4);
+          cp_async16(dst, p.latent + static_cast<int64_t>(s.idx[row]) * kD + c * 16, 16);
+        }
+        cp_async_wait_all();
+      } else {
+        for (int it = 0; it < kBK * 36 / kProdThreads; ++it) {
+          const int i = it * kProdThreads + pt;
+          const int row = i / 36, c = i - row * 36;
+          const int kc = c >> 2, c4 = c & 3;
+          const uint32_t rr = s.idx[row];
+          const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.latent + static_cast<int64_t>(rr) * kD + c * 16));
+          const float ratio = p.scales[static_cast<int64_t>(rr) * p.nscale + (c >> 1)] / s.srow[row];
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+          float x[16];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 a = e4m3x2_to_f32x2(static_cast<uint16_t>(w[k] & 0xffffu));
+            const float2 b = e4m3x2_to_f32x2(static_cast<uint16_t>(w[k] >> 16));
+            x[4 * k + 0] = a.x * ratio;
+            x[4 * k + 1] = a.y * ratio;
+            x[4 * k + 2] = b.x * ratio;
+            x[4 * k + 3] = b.y * ratio;
+          }
+          uint4 hi, lo;
+          split16(x, hi, lo);
+          const uint32_t off = kc * (kBK * 64) + row * 64 + sw64(row, c4);
+          *reinterpret_cast<uint4*>(&s.kv[0][off]) = hi;
+          *reinterpret_cast<uint4*>(&s.kv[KVP - 1][off]) = lo;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&s.bar_kv_full));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 4) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int QP, int KVP, int PP, int SC>
+static smla_status_t launch_t(const Params& p, cudaStream_t stream) {
+  const size_t smem = sizeof(Smem<QP, KVP, PP>) + 1024;
+  if (smem > 232448) return fail(SMLA_ERR_UNSUPPORTED, "prefill variant needs %zu B of shared memory", smem);
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<QP, KVP, PP, SC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return fail_cuda(e, "prefill smem attribute");
+  dim3 grid(p.T, (p.H + kNH - 1) / kNH);
+  prefill_kernel<QP, KVP, PP, SC><<<grid, kThreads, smem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "prefill launch");
+  return SMLA_OK;
+}
+
+}  // namespace pf
+
+smla_status_t launch_sparse_prefill(const void* q, int q_dtype, const uint8_t* latent, int64_t phys_rows,
+                                    const float* scales, int sbs, const uint32_t* indices, int indices_stride,
+                                    const uint32_t* topk_lengths, int T, int H, float softmax_scale, uint16_t* out,
+                                    unsigned* err, cudaStream_t stream) {
+  using namespace pf;
+  if (T > 0x7fffffff) return fail(SMLA_ERR_UNSUPPORTED, "T too large");
+  const int nscale = sbs == 0 ? 0 : (kD + sbs - 1) / sbs;
+  Params p{q, latent, phys_rows, scales, nscale, indices, indices_stride, topk_lengths, T, H, softmax_scale, out, err};
+  const bool bf16 = q_dtype == SMLA_BF16;
+  if (sbs == 0) return bf16 ? launch_t<2, 1, 2, kUnit>(p, stream) : launch_t<1, 1, 1, kUnit>(p, stream);
+  if (sbs >= kD) return bf16 ? launch_t<2, 1, 2, kRow>(p, stream) : launch_t<1, 1, 1, kRow>(p, stream);
+  if (bf16) return fail(SMLA_ERR_UNSUPPORTED, "bf16 q with block scales is not built (shared memory)");
+  return launch_t<1, 2, 1, kBlock>(p, stream);
+}
+
+}  // namespace smla

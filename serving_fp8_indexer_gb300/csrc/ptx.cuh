@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
+#include <cuda_bf16.h>
 
 #ifndef SMLA_DEVICE_INLINE
 #define SMLA_DEVICE_INLINE __device__ __forceinline__
@@ -78,6 +79,17 @@ SMLA_DEVICE_INLINE void fence_proxy_async_smem() {
 }
 SMLA_DEVICE_INLINE void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Named barrier that also ANDs a predicate over the participating threads,
+// so that a give-up decision taken by any thread is taken by all of them.
+SMLA_DEVICE_INLINE bool named_bar_and(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // ------------------------------------------------------------------ cp.async

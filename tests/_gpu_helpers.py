@@ -101,3 +101,52 @@ def sample_tokens(seqs: wl.Seqs, per_seq: int, seed=0) -> np.ndarray:
             pick |= set(rng.choice(np.arange(a + 1, e - 1), size=min(per_seq, e - a - 2), replace=False).tolist())
         out += sorted(pick)
     return np.array(out, dtype=np.int64)
+
+
+def q_attn_tensor(w: wl.Workload, dev="cuda"):
+    if w.q_dtype == wl.Q_BF16:
+        return torch.from_numpy(w.q_attn.view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(w.q_attn).to(dev)
+
+
+def run_prefill(w: wl.Workload, indices: torch.Tensor, lens: torch.Tensor, q=None):
+    dev = "cuda"
+    q = q_attn_tensor(w) if q is None else q
+    latent = torch.from_numpy(w.latent).to(dev)
+    scales = None if w.scales is None else torch.from_numpy(w.scales).to(dev)
+    out = torch.full((w.seqs.T, w.H, 512), float("nan"), dtype=torch.bfloat16, device=dev)
+    smla.sparse_prefill(q, latent, scales, w.scale_block_size, indices, lens, w.softmax_scale, out)
+    smla.check_device_errors()
+    return out
+
+
+def check_prefill(w: wl.Workload, gpu_out_rows: np.ndarray, idx_rows: np.ndarray, len_rows: np.ndarray,
+                  tokens: np.ndarray):
+    """gpu_out_rows: bf16 output rows (as float32) of `tokens`; idx/len rows
+    the indices the GPU consumed.  Returns (rel_l2, max_abs)."""
+    T = len(tokens)
+    idx_full = np.zeros((int(tokens.max()) + 1, idx_rows.shape[1]), np.uint32)
+    len_full = np.zeros(int(tokens.max()) + 1, np.uint32)
+    idx_full[tokens] = idx_rows
+    len_full[tokens] = len_rows
+    ref = oracle.sparse_prefill(w.q_attn, w.q_dtype, w.latent, w.scales, w.scale_block_size, idx_full, len_full,
+                                w.softmax_scale, tokens=tokens)
+    g = gpu_out_rows.astype(np.float64)
+    assert np.isfinite(g).all(), "non-finite attention output"
+    rel = float(np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-300))
+    mabs = float(np.abs(g - ref).max()) if T else 0.0
+    if w.q_dtype == wl.Q_BF16:
+        assert rel <= BF16_REL_L2 and mabs <= BF16_MAX_ABS, f"bf16 path: rel L2 {rel:.3g}, max abs {mabs:.3g}"
+    else:
+        assert rel <= FP8_REL_L2, f"FP8 path: rel L2 {rel:.3g} (max abs {mabs:.3g})"
+    return rel, mabs
+
+
+def rows_of(t: torch.Tensor, tokens: np.ndarray) -> np.ndarray:
+    """Selected rows of a CUDA tensor as numpy (uint32 via an int32 view)."""
+    sel = torch.from_numpy(tokens).to(t.device)
+    if t.dtype == torch.uint32:
+        return t.view(torch.int32)[sel].cpu().numpy().view(np.uint32)
+    if t.dtype == torch.bfloat16:
+        return t[sel].float().cpu().numpy()
+    return t[sel].cpu().numpy()
