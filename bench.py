@@ -1,0 +1,412 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP8 indexer -> top-k -> sparse MLA prefill path.
+
+One step = one pass of the whole path over the end-to-end prefill chunk
+(8 sequences x 8192 cached tokens, 2048 new tokens each at positions
+6144..8191; indexer H_idx=64 FP8 -> causal top-2048 -> sparse MLA with
+H=128, bf16 q, tensorwise-scaled e4m3 latent, bf16 output [16384,128,512]),
+inputs resident in HBM.  Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the float64 CPU oracle on bounded samples of the
+same workload (the path's reference arm).  Under torchrun with N > 1 every
+rank runs its own replica of the chunk (weak scaling, no collective on the
+data path); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-MLA prefill TFLOP/s (% GB300 tensor peak); indexer+topk keys·tok/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return d, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def peak_value(peaks, key):
+    v = peaks.get(key)
+    if isinstance(v, dict):
+        v = v.get("value", v.get("median"))
+    return float(v) if v is not None else FALLBACK_PEAKS[key]
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.gpu_index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- workload
+def sparse_flops(lens, H):
+    return float(sum(int(x) for x in lens)) * H * 2.0 * (576 + 512)
+
+
+def keys_tok(w):
+    from serving_fp8_indexer_gb300 import workloads as wl
+    return float((wl.token_positions(w.seqs) + 1).sum())
+
+
+CASES = {
+    # the benchmarked workload
+    "chunk": dict(),
+    # the same shapes with one sequence of 1024 new tokens (inputs still
+    # larger than L2), for ncu captures
+    "chunk_small": dict(B=1, q_len=1024),
+}
+
+
+def make_workload(case="chunk"):
+    from serving_fp8_indexer_gb300 import workloads as wl
+    return wl.e2e_chunk(**CASES[case])
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_sample(w, tokens):
+    """The float64 oracle over `tokens` of the workload (whole path);
+    returns (seconds, attention FLOPs, keys*tok of those tokens)."""
+    import numpy as np
+    import oracle
+    s = w.seqs
+    stride = int(s.kv_len.max() + 3) // 4 * 4
+    t0 = time.perf_counter()
+    sc = oracle.indexer_scores(w.q_idx, w.q_scale, w.k_pool, w.k_scale, s.cu_q, s.kv_len, s.page_table, s.page_size,
+                               stride, tokens=tokens)
+    idx, lens = oracle.topk(sc, w.topk, s.cu_q, s.kv_len, s.page_table, s.page_size, tokens=tokens)
+    full_idx = np.zeros((int(tokens.max()) + 1, w.topk), np.uint32)
+    full_len = np.zeros(int(tokens.max()) + 1, np.uint32)
+    full_idx[tokens], full_len[tokens] = idx, lens
+    oracle.sparse_prefill(w.q_attn, w.q_dtype, w.latent, w.scales, w.scale_block_size, full_idx, full_len,
+                          w.softmax_scale, tokens=tokens)
+    dt = time.perf_counter() - t0
+    from serving_fp8_indexer_gb300 import workloads as wl
+    pos = wl.token_positions(s)
+    return dt, sparse_flops(lens, w.H), float((pos[tokens] + 1).sum())
+
+
+def sample_tokens(w, n, seed=0):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(w.seqs.T, size=min(n, w.seqs.T), replace=False))
+
+
+def cpu_baseline(w, budget_s=12.0):
+    n = 4
+    dt, fl, _ = oracle_sample(w, sample_tokens(w, n, 1))
+    per_tok = dt / n
+    n2 = int(max(4, min(512, budget_s / max(per_tok, 1e-6))))
+    toks = sample_tokens(w, n2, 2)
+    dt, fl, _ = oracle_sample(w, toks)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{len(toks)} random tokens of the chunk through the float64 oracle (indexer, top-k, attention), "
+                      f"{dt:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = make_workload(args.case)
+    steps, warm = args.steps, args.warmup
+    per_step = 2
+    for i in range(warm):
+        oracle_sample(w, sample_tokens(w, per_step, 100 + i))
+    times, flops = [], []
+    for i in range(steps):
+        dt, fl, _ = oracle_sample(w, sample_tokens(w, per_step, 1000 + i))
+        times.append(dt)
+        flops.append(fl)
+    value = sum(flops) / sum(times) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": steps, "warmup": warm, "ms_per_step": 1e3 * sum(times) / steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w, world),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"{per_step} random tokens per step through the float64 oracle"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w, world):
+    B, q_len = w.seqs.B, int(w.seqs.cu_q[1])
+    return {"workload": f"end-to-end prefill chunk: {B} seqs x 8192 cached tokens, {q_len} new each "
+                        f"(the last {q_len} positions); indexer H_idx=64 fp8 -> causal top-2048 -> sparse MLA H=128, "
+                        "bf16 q, tensorwise e4m3 latent, v_depth 512",
+            "tokens": int(w.seqs.T), "H": w.H, "H_idx": w.h_idx, "topk": w.topk, "page_size": w.seqs.page_size,
+            "l2": "inputs larger than L2 (q 2.4 GB, scores 0.5 GB); the 38 MB latent pool is L2-resident by design",
+            "parallelism": f"replicas x{world}"}
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world):
+    import numpy as np
+    import torch
+
+    from serving_fp8_indexer_gb300 import build as smla_build
+    smla_build.build()
+    import serving_fp8_indexer_gb300 as smla
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    w = make_workload(args.case)
+    s = w.seqs
+    T, H, k = s.T, w.H, w.topk
+    stride = int(s.kv_len.max() + 3) // 4 * 4
+
+    seqs = smla.Seqs.from_host(s, dev)
+    q_idx = torch.from_numpy(w.q_idx).to(dev)
+    q_scale = torch.from_numpy(w.q_scale).to(dev)
+    k_pool = torch.from_numpy(w.k_pool).to(dev)
+    k_scale = torch.from_numpy(w.k_scale).to(dev)
+    latent = torch.from_numpy(w.latent).to(dev)
+    scales = torch.from_numpy(w.scales).to(dev)
+    q_attn = torch.from_numpy(w.q_attn.view(np.int16)).view(torch.bfloat16).to(dev)
+    scores = torch.empty((T, stride), device=dev)
+    idx = torch.empty((T, k), dtype=torch.uint32, device=dev)
+    lens = torch.empty((T,), dtype=torch.uint32, device=dev)
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        smla.indexer_scores(q_idx, q_scale, k_pool, k_scale, seqs, scores)
+        if ev is not None:
+            ev[1].record(stream)
+        smla.topk(scores, seqs, k, idx, lens)
+        if ev is not None:
+            ev[2].record(stream)
+        smla.sparse_prefill(q_attn, latent, scales, w.scale_block_size, idx, lens, w.softmax_scale, out)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    smla.check_device_errors()
+
+    from serving_fp8_indexer_gb300 import workloads as wl
+    pos = wl.token_positions(s)
+    flops = sparse_flops(np.minimum(pos + 1, k), H)
+    kt = float((pos + 1).sum())
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", 0)))
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    smla.check_device_errors()
+
+    total_ms = e0.elapsed_time(e1)
+    idx_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    topk_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    attn_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    if world > 1:
+        t = torch.tensor([total_ms, idx_ms, topk_ms, attn_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, idx_ms, topk_ms, attn_ms = [float(x) for x in t.tolist()]
+    ms_step = total_ms / args.steps
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    e2e = None
+    if not args.no_e2e:
+        h_qidx = torch.from_numpy(w.q_idx).pin_memory()
+        h_qs = torch.from_numpy(w.q_scale).pin_memory()
+        h_q = torch.from_numpy(w.q_attn.view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_out = torch.empty((T, H, 512), dtype=torch.bfloat16).pin_memory()
+        n_e2e = max(1, min(args.steps, 5))
+
+        def e2e_step():
+            q_idx.copy_(h_qidx, non_blocking=True)
+            q_scale.copy_(h_qs, non_blocking=True)
+            q_attn.copy_(h_q, non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = a.elapsed_time(b) / n_e2e
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        bi = h_qidx.numel() + h_qs.numel() * 4 + h_q.numel() * 2
+        bo = h_out.numel() * 2
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(bi),
+               "d2h_bytes_per_step": int(bo), "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        return
+    peaks, src = load_peaks()
+    bf16_peak = peak_value(peaks, "bf16_tflops_sustained")
+    hbm = peak_value(peaks, "hbm_gbs")
+    attn_tflops = flops / (attn_ms * 1e-3) / 1e12
+    frac = attn_tflops / bf16_peak
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        try:
+            traffic = json.load(open(prof)).get("prefill_kernel_bytes_per_launch")
+        except Exception:
+            traffic = None
+    idx_bytes = q_idx.numel() + q_scale.numel() * 4 + k_pool.numel() + k_scale.numel() * 4 + 4 * kt
+    topk_bytes = 4 * kt + 4 * T * k + 4 * T
+    line = {
+        "metric": METRIC,
+        "value": world * flops / (ms_step * 1e-3) / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 MMA (bf16 q and P as e4m3 hi+lo), f32 accumulate",
+        "data": "synthetic",
+        "config": config_dict(w, world),
+        "stages": {
+            "indexer": {"ms": idx_ms, "TFLOP/s": 1e-12 * kt * w.h_idx * 256 / (idx_ms * 1e-3),
+                        "GB/s_algorithmic": 1e-9 * idx_bytes / (idx_ms * 1e-3)},
+            "topk": {"ms": topk_ms, "GB/s_algorithmic": 1e-9 * topk_bytes / (topk_ms * 1e-3),
+                     "frac_hbm": 1e-9 * topk_bytes / (topk_ms * 1e-3) / hbm},
+            "sparse_mla": {"ms": attn_ms, "TFLOP/s": attn_tflops, "frac_bf16_peak": frac},
+        },
+        "indexer_topk": {"value": world * kt / ((idx_ms + topk_ms) * 1e-3), "unit": "keys·tok/s"},
+        "roofline": {"bound": "tensor", "kernel": "prefill_kernel (sparse MLA)", "achieved": attn_tflops,
+                     "peak": bf16_peak, "unit": "TFLOP/s", "frac": frac, "traffic": traffic,
+                     "peak_source": f"{src} bf16 dense (sustained)"},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=sorted(CASES), default="chunk")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

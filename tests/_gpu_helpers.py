@@ -135,6 +135,7 @@ def check_prefill(w: wl.Workload, gpu_out_rows: np.ndarray, idx_rows: np.ndarray
     assert np.isfinite(g).all(), "non-finite attention output"
     rel = float(np.linalg.norm(g - ref) / max(np.linalg.norm(ref), 1e-300))
     mabs = float(np.abs(g - ref).max()) if T else 0.0
+    print(f"[prefill parity] {w.name}: {T} tokens, rel L2 {rel:.3e}, max abs {mabs:.3e}")
     if w.q_dtype == wl.Q_BF16:
         assert rel <= BF16_REL_L2 and mabs <= BF16_MAX_ABS, f"bf16 path: rel L2 {rel:.3g}, max abs {mabs:.3g}"
     else:
