@@ -29,13 +29,20 @@
 // normaliser sums exp2(z - m), so out = sum_j p_j s_j Vraw_j / sum_j p_j.
 //
 // Softmax: keys are TMEM lanes, so a head's maximum is a cross-lane
-// reduction (warp redux on order-preserving ints, then across 4 warps).
-// The reference maximum m is only raised when a block exceeds it by more
-// than 2^8 (lazy rescale), keeping P <= 256 inside the e4m3 range; raising
-// it rescales O^T and the row sums.
+// reduction (warp redux on order-preserving ints, then shared-memory atomic
+// max across the 4 lane quarters).  The reference maximum m is only raised
+// when a block exceeds it by more than 2^8 (lazy rescale), keeping P <= 256
+// inside the e4m3 range; raising it rescales O^T and the row sums.
 //
-// Warp roles: warps 0-3 softmax / epilogue (thread = key lane), warp 4
-// MMA issuer and TMEM owner, warps 5-7 gather producers.
+// Pipeline: NST gather slots (2 when they fit in shared memory).  Block
+// j+1's rows are gathered while block j goes through QK, softmax and PV.
+// The rope chunk of a slot (columns 512..575) is dead once QK has read it,
+// so the block's P (hi term) is written there; only the bf16 path's P lo
+// term needs a buffer of its own.
+//
+// Warp roles: warps 0-7 softmax / epilogue (lane quarter w%4, head half
+// w/4; thread = one key x 32 heads), warp 8 MMA issuer and TMEM owner,
+// warps 9-11 gather producers.
 #include <algorithm>
 
 #include "ptx.cuh"
@@ -44,21 +51,26 @@
 namespace smla {
 namespace pf {
 
-constexpr int kD = 576;          // qk depth
-constexpr int kDV = 512;         // v depth
-constexpr int kNH = 64;          // heads per CTA (MMA N)
-constexpr int kBK = 128;         // keys per block (MMA M of QK)
-constexpr int kChunks = kD / 64; // 64-byte K chunks per row (SW64)
-constexpr int kQBytes = kChunks * kNH * 64;     // 36864
-constexpr int kKVBytes = kChunks * kBK * 64;    // 73728
-constexpr int kPBytes = kBK * kNH;              // 8192
-constexpr int kThreads = 256;
-constexpr int kSoftThreads = 128;
+constexpr int kD = 576;           // qk depth
+constexpr int kDV = 512;          // v depth
+constexpr int kNH = 64;           // heads per CTA (MMA N)
+constexpr int kBK = 128;          // keys per block (MMA M of QK)
+constexpr int kChunks = kD / 64;  // 64-byte K chunks per row (SW64)
+constexpr int kQBytes = kChunks * kNH * 64;   // 36864
+constexpr int kKVBytes = kChunks * kBK * 64;  // 73728
+constexpr int kChunkBytes = kBK * 64;         // 8192: one 64-column chunk of a block
+constexpr int kRope = 8;                      // chunk index of columns 512..575
+constexpr int kSoftWarps = 8;
+constexpr int kSoftThreads = kSoftWarps * 32;
+constexpr int kMmaWarp = 8;
+constexpr int kProdWarp0 = 9;
 constexpr int kProdThreads = 96;
+constexpr int kThreads = kSoftThreads + 32 + kProdThreads;  // 384
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 256;  // S^T columns [256, 320); O^T tiles at [0, 256)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTau = 8.0f;      // lazy-rescale threshold (log2 units)
+constexpr int kOrdMin = static_cast<int>(0x80000000u);
 
 enum Scale { kUnit = 0, kRow = 1, kBlock = 2 };
 
@@ -77,21 +89,19 @@ struct Params {
   unsigned* err;
 };
 
-template <int QP, int KVP, int PP>
+template <int QP, int KVP, int PP, int NST>
 struct Smem {
   uint8_t q[QP][kQBytes];
-  uint8_t kv[KVP][kKVBytes];
-  uint8_t p[PP][kPBytes];
+  uint8_t kv[NST][KVP][kKVBytes];
+  uint8_t plo[(PP == 2 && KVP == 1) ? kChunkBytes : 16];  // P lo when no rope-lo chunk holds it
   uint32_t idx[kBK];
-  float srow[kBK];       // per-row scale (1 for unit)
-  float lgrow[kBK];      // log2 of it
+  float srow[NST][kBK];  // per-row scale (1 for unit)
   float cs[kNH];         // softmax_scale * log2(e) / 2^e_h
   float mref[kNH];       // reference maximum per head (log2 units)
-  float fac[kNH];        // rescale factor of the current block
-  float red[4][kNH];     // cross-warp scratch
-  float linv[kNH];
-  int rescale;
-  unsigned long long bar_q, bar_kv_full, bar_kv_empty, bar_s_full, bar_p_full;
+  float fac[kNH];        // rescale factor of the current block; row sums at the end
+  int mx[2][kNH];        // block maximum per head (order-preserving ints), by block parity
+  int rescale[2];
+  unsigned long long bar_q, bar_kv_full[NST], bar_kv_empty[NST], bar_s_full, bar_p_full, bar_pv_done;
   uint32_t tmem_base;
 };
 
@@ -119,16 +129,29 @@ __device__ __forceinline__ void split16(const float (&x)[16], uint4& hi, uint4& 
   hi = make_uint4(h[0], h[1], h[2], h[3]);
   lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
+__device__ __forceinline__ uint4 quant16(const float (&x)[16]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = static_cast<uint32_t>(f32x2_to_e4m3x2(x[4 * i], x[4 * i + 1])) |
+           (static_cast<uint32_t>(f32x2_to_e4m3x2(x[4 * i + 2], x[4 * i + 3])) << 16);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
-template <int QP, int KVP, int PP, int SC>
+template <int QP, int KVP, int PP, int NST, int SC>
 __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
-  using S = Smem<QP, KVP, PP>;
-  extern __shared__ uint8_t smem_raw[];
-  S& s = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using S = Smem<QP, KVP, PP, NST>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The swizzled operand tiles need 1024-byte alignment; the launch asks
+  // for exactly sizeof(S) bytes, so the dynamic window must start aligned.
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrShape);
+    return;
+  }
+  S& s = *reinterpret_cast<S*>(smem_raw);
   const int t = blockIdx.x;
-  const int g = blockIdx.y;
-  const int h0 = g * kNH;
+  const int h0 = blockIdx.y * kNH;
   const int hv = min(kNH, p.H - h0);  // valid heads of this CTA
   int n = static_cast<int>(p.lens[t]);
   if (n > p.indices_stride) {
@@ -146,14 +169,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&s.bar_q), kSoftThreads);
-    mbar_init(smem_u32(&s.bar_kv_full), kProdThreads);
-    mbar_init(smem_u32(&s.bar_kv_empty), 1);
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(smem_u32(&s.bar_kv_full[i]), kProdThreads);
+      mbar_init(smem_u32(&s.bar_kv_empty[i]), 1);
+    }
     mbar_init(smem_u32(&s.bar_s_full), 1);
     mbar_init(smem_u32(&s.bar_p_full), kSoftThreads);
-    s.rescale = 0;
+    mbar_init(smem_u32(&s.bar_pv_done), 1);
+    s.rescale[0] = s.rescale[1] = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (threadIdx.x < 2 * kNH) (&s.mx[0][0])[threadIdx.x] = kOrdMin;
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&s.tmem_base), kTmemCols);
     tmem_relinquish();
   }
@@ -162,20 +189,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
 
-  if (warp < 4) {
+  if (warp < kSoftWarps) {
     // =================================================================== softmax / epilogue
-    const int r = threadIdx.x;  // key lane 0..127
-    // ---- Q: 2 threads per head, 288 elements each, as 18 groups of 16
+    const int r = threadIdx.x & 127;        // key lane = TMEM lane
+    const int half = warp >> 2;             // heads [32*half, 32*half + 32)
+    const int hb = half * 32;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    // ---- Q: 4 threads per head, 144 elements each, as 9 groups of 16
     {
-      const int hh = r >> 1, half = r & 1;
+      const int hh = threadIdx.x >> 2, qtr = threadIdx.x & 3;
       const bool hvalid = hh < hv;
       float sigma = 1.f;
       if (QP == 2) {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                          (static_cast<int64_t>(t) * p.H + h0 + hh) * kD + half * 288);
+                                                          (static_cast<int64_t>(t) * p.H + h0 + hh) * kD + qtr * 144);
         float amax = 0.f;
         if (hvalid)
-          for (int i = 0; i < 36; ++i) {
+          for (int i = 0; i < 18; ++i) {
             const uint4 v = __ldg(src + i);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -185,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
             }
           }
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         // scale so that the largest |q| * 2^e lies in [128, 256)
         int e = 0;
         if (amax > 0.f) {
@@ -193,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
           e = 8 - ex;
         }
         sigma = ldexpf(1.f, e);
-        for (int i = 0; i < 18; ++i) {
+        for (int i = 0; i < 9; ++i) {
           float x[16];
           if (hvalid) {
             const uint4 a = __ldg(src + 2 * i), b = __ldg(src + 2 * i + 1);
@@ -209,23 +240,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
           }
           uint4 hi, lo;
           split16(x, hi, lo);
-          const int e0 = half * 288 + 16 * i;
+          const int e0 = qtr * 144 + 16 * i;
           const int kc = e0 >> 6, c4 = (e0 & 63) >> 4;
           const uint32_t off = kc * (kNH * 64) + hh * 64 + sw64(hh, c4);
           *reinterpret_cast<uint4*>(&s.q[0][off]) = hi;
-          *reinterpret_cast<uint4*>(&s.q[1 % QP][off]) = lo;
+          *reinterpret_cast<uint4*>(&s.q[QP - 1][off]) = lo;
         }
       } else {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) +
-                                                          (static_cast<int64_t>(t) * p.H + h0 + hh) * kD + half * 288);
-        for (int i = 0; i < 18; ++i) {
+                                                          (static_cast<int64_t>(t) * p.H + h0 + hh) * kD + qtr * 144);
+        for (int i = 0; i < 9; ++i) {
           const uint4 v = hvalid ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
-          const int e0 = half * 288 + 16 * i;
+          const int e0 = qtr * 144 + 16 * i;
           const int kc = e0 >> 6, c4 = (e0 & 63) >> 4;
           *reinterpret_cast<uint4*>(&s.q[0][kc * (kNH * 64) + hh * 64 + sw64(hh, c4)]) = v;
         }
       }
-      if (half == 0) {
+      if (qtr == 0) {
         s.cs[hh] = p.softmax_scale * kLog2e / sigma;
         s.mref[hh] = -INFINITY;
       }
@@ -234,108 +265,103 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
     }
     named_bar_sync(1, kSoftThreads);
 
-    float lpart[kNH];
+    float lpart[32];
 #pragma unroll
-    for (int h = 0; h < kNH; ++h) lpart[h] = 0.f;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    for (int h = 0; h < 32; ++h) lpart[h] = 0.f;
     bool ok = true;
 
     for (int j = 0; ok && j < nblk; ++j) {
+      const int slot = j % NST;
       // S^T of block j is ready; kv_full is also waited so that the
       // producers' per-row scales are visible to this thread.
       bool w = mbar_wait(smem_u32(&s.bar_s_full), j & 1, p.err) &&
-               mbar_wait(smem_u32(&s.bar_kv_full), j & 1, p.err);
+               mbar_wait(smem_u32(&s.bar_kv_full[slot]), (j / NST) & 1, p.err);
       if (!named_bar_and(1, kSoftThreads, w)) { ok = false; break; }
       tc_fence_after();
-      float z[kNH];
+      float z[32];
       {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kTmemS, v);
+        tmem_ld32(tmem + lane_base + kTmemS + hb, v);
         tmem_wait_ld();
 #pragma unroll
         for (int h = 0; h < 32; ++h) z[h] = __uint_as_float(v[h]);
-        tmem_ld32(tmem + lane_base + kTmemS + 32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int h = 0; h < 32; ++h) z[32 + h] = __uint_as_float(v[h]);
       }
       tc_fence_before();
       const bool valid = j * kBK + r < n;
-      const float sr = s.srow[r];
-      const float lg = s.lgrow[r];
+      const float sr = s.srow[slot][r];
+      const float lg = SC == kUnit ? 0.f : __log2f(sr);
       // z = logit in log2 units; w = z + log2(s_row) is the PV operand's exponent
-      int mine0 = 0, mine1 = 0;
+      int mine = kOrdMin;
 #pragma unroll
-      for (int h = 0; h < kNH; ++h) {
-        z[h] = valid ? z[h] * sr * s.cs[h] : -INFINITY;
+      for (int h = 0; h < 32; ++h) {
+        z[h] = valid ? z[h] * sr * s.cs[hb + h] : -INFINITY;
         const int m = __reduce_max_sync(0xffffffffu, ord_int(z[h] + lg));
-        if (h < 32) { if (lane == h) mine0 = m; } else { if (lane == h - 32) mine1 = m; }
+        if (lane == h) mine = m;
       }
-      s.red[warp][lane] = ord_float(mine0);
-      s.red[warp][32 + lane] = ord_float(mine1);
+      atomicMax(&s.mx[j & 1][hb + lane], mine);
       named_bar_sync(1, kSoftThreads);
-      if (r < kNH) {
-        const float mb = fmaxf(fmaxf(s.red[0][r], s.red[1][r]), fmaxf(s.red[2][r], s.red[3][r]));
-        const float old = s.mref[r];
+      if ((warp & 3) == 0) {
+        const int hh = hb + lane;
+        const float mb = ord_float(s.mx[j & 1][hh]);
+        s.mx[(j + 1) & 1][hh] = kOrdMin;
+        const float old = s.mref[hh];
         float f = 1.f;
         if (mb > old + kTau) {
-          s.mref[r] = mb;
+          s.mref[hh] = mb;
           f = exp2f(old - mb);  // 0 when old is -inf
-          if (j > 0) s.rescale = 1;
+          if (j > 0) s.rescale[j & 1] = 1;
         }
-        s.fac[r] = f;
+        s.fac[hh] = f;
+        if (hh == 0) s.rescale[(j + 1) & 1] = 0;
       }
       named_bar_sync(1, kSoftThreads);
-      const bool rescale = s.rescale != 0;
-      if (rescale) {
+      if (s.rescale[j & 1]) {
         // O^T holds blocks < j: wait for the last PV, then scale each head's column.
-        w = mbar_wait(smem_u32(&s.bar_kv_empty), (j - 1) & 1, p.err);
+        w = mbar_wait(smem_u32(&s.bar_pv_done), (j - 1) & 1, p.err);
         if (!named_bar_and(1, kSoftThreads, w)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
         for (int tile = 0; tile < 4; ++tile) {
+          uint32_t v[32];
+          const uint32_t a = tmem + lane_base + tile * kNH + hb;
+          tmem_ld32(a, v);
+          tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t v[32];
-            const uint32_t a = tmem + lane_base + tile * kNH + c * 32;
-            tmem_ld32(a, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int h = 0; h < 32; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * s.fac[c * 32 + h]);
-            tmem_st32(a, v);
-          }
+          for (int h = 0; h < 32; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * s.fac[hb + h]);
+          tmem_st32(a, v);
         }
         tmem_wait_st();
         tc_fence_before();
       }
 #pragma unroll
-      for (int h = 0; h < kNH; ++h) lpart[h] *= s.fac[h];
-      named_bar_sync(1, kSoftThreads);
-      if (r == 0) s.rescale = 0;
-      // ---- P (row r of the [key][head] buffers), row sums
+      for (int h = 0; h < 32; ++h) lpart[h] *= s.fac[hb + h];
+      // ---- P row r (this thread's 32 heads) and the row sums
+      if (PP == 2 && KVP == 1 && j > 0) {
+        // the single P-lo buffer is still read by PV of block j-1
+        w = mbar_wait(smem_u32(&s.bar_pv_done), (j - 1) & 1, p.err);
+        if (!named_bar_and(1, kSoftThreads, w)) { ok = false; break; }
+      }
       const float isr = 1.f / sr;
+      uint8_t* p_hi = &s.kv[slot][0][kRope * kChunkBytes];
+      uint8_t* p_lo = (KVP == 2) ? &s.kv[slot][KVP - 1][kRope * kChunkBytes] : s.plo;
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c = 0; c < 2; ++c) {
         float x[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const int h = c4 * 16 + k;
-          const float pw = exp2f(z[h] + lg - s.mref[h]);   // 0 for invalid rows
+          const int h = c * 16 + k;
+          const float pw = exp2f(z[h] + lg - s.mref[hb + h]);   // 0 for invalid rows
           x[k] = pw;
           lpart[h] += pw * isr;
         }
+        const int c4 = half * 2 + c;
         if (PP == 2) {
           uint4 hi, lo;
           split16(x, hi, lo);
-          *reinterpret_cast<uint4*>(&s.p[0][r * 64 + sw64(r, c4)]) = hi;
-          *reinterpret_cast<uint4*>(&s.p[PP - 1][r * 64 + sw64(r, c4)]) = lo;
+          *reinterpret_cast<uint4*>(p_hi + r * 64 + sw64(r, c4)) = hi;
+          *reinterpret_cast<uint4*>(p_lo + r * 64 + sw64(r, c4)) = lo;
         } else {
-          uint32_t w[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            w[i] = static_cast<uint32_t>(f32x2_to_e4m3x2(x[4 * i], x[4 * i + 1])) |
-                   (static_cast<uint32_t>(f32x2_to_e4m3x2(x[4 * i + 2], x[4 * i + 3])) << 16);
-          *reinterpret_cast<uint4*>(&s.p[0][r * 64 + sw64(r, c4)]) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(p_hi + r * 64 + sw64(r, c4)) = quant16(x);
         }
       }
       fence_proxy_async_smem();
@@ -343,52 +369,47 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
     }
 
     // ---- row sums across the 128 key lanes, then O^T / l -> bf16
+    const bool done =
+        named_bar_and(1, kSoftThreads, ok && mbar_wait(smem_u32(&s.bar_pv_done), (nblk - 1) & 1, p.err));
+    float* lsum = s.fac;  // reused as the row-sum accumulator
+    if (threadIdx.x < kNH) lsum[threadIdx.x] = 0.f;
+    named_bar_sync(1, kSoftThreads);
 #pragma unroll
-    for (int h = 0; h < kNH; ++h) {
+    for (int h = 0; h < 32; ++h) {
       float v = lpart[h];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      lpart[h] = v;
-    }
-    if (lane == 0)
-#pragma unroll
-      for (int h = 0; h < kNH; ++h) s.red[warp][h] = lpart[h];
-    named_bar_sync(1, kSoftThreads);
-    if (r < kNH) {
-      const float l = s.red[0][r] + s.red[1][r] + s.red[2][r] + s.red[3][r];
-      s.linv[r] = l > 0.f ? 1.f / l : 0.f;
+      if (lane == 0) atomicAdd(&lsum[hb + h], v);
     }
     named_bar_sync(1, kSoftThreads);
-    const bool done = named_bar_and(1, kSoftThreads, ok && mbar_wait(smem_u32(&s.bar_kv_empty), (nblk - 1) & 1, p.err));
     if (done) {
       tc_fence_after();
 #pragma unroll 1
       for (int tile = 0; tile < 4; ++tile) {
         const int vcol = tile * 128 + r;
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + tile * kNH + hb, v);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + tile * kNH + c * 32, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int h = 0; h < 32; ++h) {
-            const int hh = c * 32 + h;
-            if (hh < hv) {
-              const float o = __uint_as_float(v[h]) * s.linv[hh];
-              out_t[static_cast<int64_t>(hh) * kDV + vcol] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
-            }
+        for (int h = 0; h < 32; ++h) {
+          const int head = hb + h;
+          if (head < hv) {
+            const float l = lsum[head];
+            const float o = l > 0.f ? __uint_as_float(v[h]) / l : 0.f;
+            out_t[static_cast<int64_t>(head) * kDV + vcol] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
           }
         }
       }
     }
-  } else if (warp == 4) {
+  } else if (warp == kMmaWarp) {
     // =================================================================== MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_e4m3_f32(kBK, kNH, 0, 0);
       constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, kNH, 1, 1);
       bool ok = mbar_wait(smem_u32(&s.bar_q), 0, p.err);
       for (int j = 0; ok && j < nblk; ++j) {
-        if (!mbar_wait(smem_u32(&s.bar_kv_full), j & 1, p.err)) break;
+        const int slot = j % NST;
+        if (!mbar_wait(smem_u32(&s.bar_kv_full[slot]), (j / NST) & 1, p.err)) break;
         tc_fence_after();
         uint32_t acc = 0;
 #pragma unroll 1
@@ -399,7 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
             for (int kc = 0; kc < kChunks; ++kc)
 #pragma unroll
               for (int kk = 0; kk < 2; ++kk) {
-                const uint64_t ad = make_sdesc(smem_u32(s.kv[kp]) + kc * (kBK * 64) + kk * 32, 16, 512, kSwizzle64B);
+                const uint64_t ad =
+                    make_sdesc(smem_u32(s.kv[slot][kp]) + kc * kChunkBytes + kk * 32, 16, 512, kSwizzle64B);
                 const uint64_t bd = make_sdesc(smem_u32(s.q[qp]) + kc * (kNH * 64) + kk * 32, 16, 512, kSwizzle64B);
                 mma_f8f6f4_ss(tmem + kTmemS, ad, bd, IDESC_QK, acc);
                 acc = 1;
@@ -407,6 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
         mma_commit(smem_u32(&s.bar_s_full));
         if (!mbar_wait(smem_u32(&s.bar_p_full), j & 1, p.err)) break;
         tc_fence_after();
+        const uint32_t p_hi = smem_u32(&s.kv[slot][0][kRope * kChunkBytes]);
+        const uint32_t p_lo = (KVP == 2) ? smem_u32(&s.kv[slot][KVP - 1][kRope * kChunkBytes]) : smem_u32(s.plo);
 #pragma unroll 1
         for (int tile = 0; tile < 4; ++tile) {
           uint32_t pacc = j > 0 ? 1u : 0u;
@@ -416,24 +440,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
             for (int kp = 0; kp < KVP; ++kp)
 #pragma unroll
               for (int ks = 0; ks < kBK / 32; ++ks) {
-                const uint64_t ad =
-                    make_sdesc(smem_u32(s.kv[kp]) + (2 * tile) * (kBK * 64) + ks * 32 * 64, kBK * 64, 512, kSwizzle64B);
-                const uint64_t bd = make_sdesc(smem_u32(s.p[pp]) + ks * 32 * 64, kBK * 64, 512, kSwizzle64B);
+                const uint64_t ad = make_sdesc(smem_u32(s.kv[slot][kp]) + (2 * tile) * kChunkBytes + ks * 32 * 64,
+                                               kChunkBytes, 512, kSwizzle64B);
+                const uint64_t bd = make_sdesc((pp == 0 ? p_hi : p_lo) + ks * 32 * 64, kChunkBytes, 512, kSwizzle64B);
                 mma_f8f6f4_ss(tmem + tile * kNH, ad, bd, IDESC_PV, pacc);
                 pacc = 1;
               }
         }
-        mma_commit(smem_u32(&s.bar_kv_empty));
+        mma_commit(smem_u32(&s.bar_kv_empty[slot]));
+        mma_commit(smem_u32(&s.bar_pv_done));
       }
     }
   } else {
     // =================================================================== gather producers
-    const int pt = threadIdx.x - 160;  // 0..95
+    const int pt = threadIdx.x - kProdWarp0 * 32;  // 0..95
     const uint32_t first = tok_idx[0];
     for (int j = 0; j < nblk; ++j) {
-      const bool w = mbar_wait(smem_u32(&s.bar_kv_empty), (j & 1) ^ 1, p.err);
+      const int slot = j % NST;
+      const bool w = mbar_wait(smem_u32(&s.bar_kv_empty[slot]), ((j / NST) & 1) ^ 1, p.err);
       if (!named_bar_and(2, kProdThreads, w)) break;
-      // rows pt, pt+96 of this block: physical row and scale
+      // rows of this block: physical row and scale
       for (int rr = pt; rr < kBK; rr += kProdThreads) {
         const int key = j * kBK + rr;
         uint32_t row = key < n ? tok_idx[key] : first;
@@ -451,8 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
           for (int b = 0; b < p.nscale; ++b) sr = fmaxf(sr, sp[b]);
           if (!(sr > 0.f)) sr = 1.f;
         }
-        s.srow[rr] = sr;
-        s.lgrow[rr] = SC == kUnit ? 0.f : log2f(sr);
+        s.srow[slot][rr] = sr;
       }
       named_bar_sync(2, kProdThreads);
       if (KVP == 1) {
@@ -461,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
           const int i = it * kProdThreads + pt;
           const int row = i / 36, c = i - row * 36;
           const int kc = c >> 2, c4 = c & 3;
-          const uint32_t dst = smem_u32(s.kv[0]) + kc * (kBK * 64) + row * 64 + sw64(row, c4);
+          const uint32_t dst = smem_u32(s.kv[slot][0]) + kc * kChunkBytes + row * 64 + sw64(row, c4);
           cp_async16(dst, p.latent + static_cast<int64_t>(s.idx[row]) * kD + c * 16, 16);
         }
         cp_async_wait_all();
@@ -472,13 +497,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
           const int kc = c >> 2, c4 = c & 3;
           const uint32_t rr = s.idx[row];
           const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.latent + static_cast<int64_t>(rr) * kD + c * 16));
-          const float ratio = p.scales[static_cast<int64_t>(rr) * p.nscale + (c >> 1)] / s.srow[row];
-          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+          const float ratio = p.scales[static_cast<int64_t>(rr) * p.nscale + (c >> 1)] / s.srow[slot][row];
+          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
           float x[16];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float2 a = e4m3x2_to_f32x2(static_cast<uint16_t>(w[k] & 0xffffu));
-            const float2 b = e4m3x2_to_f32x2(static_cast<uint16_t>(w[k] >> 16));
+            const float2 a = e4m3x2_to_f32x2(static_cast<uint16_t>(wv[k] & 0xffffu));
+            const float2 b = e4m3x2_to_f32x2(static_cast<uint16_t>(wv[k] >> 16));
             x[4 * k + 0] = a.x * ratio;
             x[4 * k + 1] = a.y * ratio;
             x[4 * k + 2] = b.x * ratio;
@@ -486,31 +511,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
           }
           uint4 hi, lo;
           split16(x, hi, lo);
-          const uint32_t off = kc * (kBK * 64) + row * 64 + sw64(row, c4);
-          *reinterpret_cast<uint4*>(&s.kv[0][off]) = hi;
-          *reinterpret_cast<uint4*>(&s.kv[KVP - 1][off]) = lo;
+          const uint32_t off = kc * kChunkBytes + row * 64 + sw64(row, c4);
+          *reinterpret_cast<uint4*>(&s.kv[slot][0][off]) = hi;
+          *reinterpret_cast<uint4*>(&s.kv[slot][KVP - 1][off]) = lo;
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&s.bar_kv_full));
+      mbar_arrive(smem_u32(&s.bar_kv_full[slot]));
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int QP, int KVP, int PP, int SC>
+template <int QP, int KVP, int PP, int NST, int SC>
 static smla_status_t launch_t(const Params& p, cudaStream_t stream) {
-  const size_t smem = sizeof(Smem<QP, KVP, PP>) + 1024;
+  const size_t smem = sizeof(Smem<QP, KVP, PP, NST>);
   if (smem > 232448) return fail(SMLA_ERR_UNSUPPORTED, "prefill variant needs %zu B of shared memory", smem);
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<QP, KVP, PP, SC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<QP, KVP, PP, NST, SC>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return fail_cuda(e, "prefill smem attribute");
   dim3 grid(p.T, (p.H + kNH - 1) / kNH);
-  prefill_kernel<QP, KVP, PP, SC><<<grid, kThreads, smem, stream>>>(p);
+  prefill_kernel<QP, KVP, PP, NST, SC><<<grid, kThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, "prefill launch");
   return SMLA_OK;
@@ -523,14 +548,13 @@ smla_status_t launch_sparse_prefill(const void* q, int q_dtype, const uint8_t* l
                                     const uint32_t* topk_lengths, int T, int H, float softmax_scale, uint16_t* out,
                                     unsigned* err, cudaStream_t stream) {
   using namespace pf;
-  if (T > 0x7fffffff) return fail(SMLA_ERR_UNSUPPORTED, "T too large");
   const int nscale = sbs == 0 ? 0 : (kD + sbs - 1) / sbs;
   Params p{q, latent, phys_rows, scales, nscale, indices, indices_stride, topk_lengths, T, H, softmax_scale, out, err};
   const bool bf16 = q_dtype == SMLA_BF16;
-  if (sbs == 0) return bf16 ? launch_t<2, 1, 2, kUnit>(p, stream) : launch_t<1, 1, 1, kUnit>(p, stream);
-  if (sbs >= kD) return bf16 ? launch_t<2, 1, 2, kRow>(p, stream) : launch_t<1, 1, 1, kRow>(p, stream);
+  if (sbs == 0) return bf16 ? launch_t<2, 1, 2, 2, kUnit>(p, stream) : launch_t<1, 1, 1, 2, kUnit>(p, stream);
+  if (sbs >= kD) return bf16 ? launch_t<2, 1, 2, 2, kRow>(p, stream) : launch_t<1, 1, 1, 2, kRow>(p, stream);
   if (bf16) return fail(SMLA_ERR_UNSUPPORTED, "bf16 q with block scales is not built (shared memory)");
-  return launch_t<1, 2, 1, kBlock>(p, stream);
+  return launch_t<1, 2, 1, 1, kBlock>(p, stream);
 }
 
 }  // namespace smla
