@@ -37,7 +37,7 @@ smla_status_t fail_cuda(cudaError_t e, const char* what) {
 }
 
 bool encode_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-                      uint32_t box_rows) {
+                      uint32_t box_rows, int swizzle_bytes) {
   const cuuint64_t dims[2] = {inner, rows};
   const cuuint64_t strides[1] = {inner};
   const cuuint32_t box[2] = {box_inner, box_rows};
@@ -61,7 +61,8 @@ bool encode_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64
     }
   }
   const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

@@ -42,7 +42,8 @@
 //
 // Warp roles: warps 0-7 softmax / epilogue (lane quarter w%4, head half
 // w/4; thread = one key x 32 heads), warp 8 MMA issuer and TMEM owner,
-// warps 9-11 gather producers.
+// warps 9-11 gather producers (cp.async 16 B into the SW64 layout, or a
+// register dequantisation of blockwise rows).
 #include <algorithm>
 
 #include "ptx.cuh"
@@ -64,8 +65,9 @@ constexpr int kSoftWarps = 8;
 constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kMmaWarp = 8;
 constexpr int kProdWarp0 = 9;
-constexpr int kProdThreads = 96;
-constexpr int kThreads = kSoftThreads + 32 + kProdThreads;  // 384
+// Three producer warps gather (cp.async), or dequantise blockwise rows.
+__host__ __device__ constexpr int prod_warps(int) { return 3; }
+__host__ __device__ constexpr int threads_for(int kvp) { return kSoftThreads + 32 + 32 * prod_warps(kvp); }
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 256;  // S^T columns [256, 320); O^T tiles at [0, 256)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -113,18 +115,20 @@ __device__ __forceinline__ float ord_float(int o) { return __int_as_float(o >= 0
 
 __device__ __forceinline__ uint32_t sw64(int row, int c4) { return static_cast<uint32_t>((c4 ^ ((row >> 1) & 3)) << 4); }
 
-// e4m3 hi + lo split of 16 floats into two 16-byte chunks.
+// e4m3 hi + lo split of 16 floats (|x| <= 448) into two 16-byte chunks.
+// The residual is formed in f16x2: x -> f16 (2^-11), hi = e4m3(x_f16),
+// lo = e4m3(x_f16 - hi) (exact subtraction); |x - hi - lo| <~ 2^-9 |x|.
 __device__ __forceinline__ void split16(const float (&x)[16], uint4& hi, uint4& lo) {
   uint32_t h[4], l[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint16_t h0 = f32x2_to_e4m3x2(x[4 * i + 0], x[4 * i + 1]);
-    const uint16_t h1 = f32x2_to_e4m3x2(x[4 * i + 2], x[4 * i + 3]);
-    const float2 b0 = e4m3x2_to_f32x2(h0), b1 = e4m3x2_to_f32x2(h1);
-    const uint16_t l0 = f32x2_to_e4m3x2(x[4 * i + 0] - b0.x, x[4 * i + 1] - b0.y);
-    const uint16_t l1 = f32x2_to_e4m3x2(x[4 * i + 2] - b1.x, x[4 * i + 3] - b1.y);
-    h[i] = static_cast<uint32_t>(h0) | (static_cast<uint32_t>(h1) << 16);
-    l[i] = static_cast<uint32_t>(l0) | (static_cast<uint32_t>(l1) << 16);
+    const uint32_t a = f32x2_to_f16x2(x[4 * i + 0], x[4 * i + 1]);
+    const uint32_t b = f32x2_to_f16x2(x[4 * i + 2], x[4 * i + 3]);
+    const uint16_t ha = f16x2_to_e4m3x2(a), hb = f16x2_to_e4m3x2(b);
+    const uint16_t la = f16x2_to_e4m3x2(hsub2(a, e4m3x2_to_f16x2(ha)));
+    const uint16_t lb = f16x2_to_e4m3x2(hsub2(b, e4m3x2_to_f16x2(hb)));
+    h[i] = static_cast<uint32_t>(ha) | (static_cast<uint32_t>(hb) << 16);
+    l[i] = static_cast<uint32_t>(la) | (static_cast<uint32_t>(lb) << 16);
   }
   hi = make_uint4(h[0], h[1], h[2], h[3]);
   lo = make_uint4(l[0], l[1], l[2], l[3]);
@@ -139,8 +143,11 @@ __device__ __forceinline__ uint4 quant16(const float (&x)[16]) {
 }
 
 template <int QP, int KVP, int PP, int NST, int SC>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
+__global__ void __launch_bounds__(threads_for(KVP), 1)
+    prefill_kernel(const Params p) {
   using S = Smem<QP, KVP, PP, NST>;
+  constexpr int kThreads = threads_for(KVP);
+  constexpr int kProdThreads = 32 * prod_warps(KVP);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // The swizzled operand tiles need 1024-byte alignment; the launch asks
@@ -288,53 +295,61 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
       }
       tc_fence_before();
       const bool valid = j * kBK + r < n;
-      const float sr = s.srow[slot][r];
+      const float sr = SC == kUnit ? 1.f : s.srow[slot][r];
       const float lg = SC == kUnit ? 0.f : __log2f(sr);
-      // z = logit in log2 units; w = z + log2(s_row) is the PV operand's exponent
-      int mine = kOrdMin;
+      // z = logit in log2 units; z + log2(s_row) is the PV operand's exponent.
+      // Fast path: no element exceeds its head's reference by more than tau.
+      bool ex = false;
 #pragma unroll
       for (int h = 0; h < 32; ++h) {
-        z[h] = valid ? z[h] * sr * s.cs[hb + h] : -INFINITY;
-        const int m = __reduce_max_sync(0xffffffffu, ord_int(z[h] + lg));
-        if (lane == h) mine = m;
+        z[h] = valid ? z[h] * (sr * s.cs[hb + h]) : -INFINITY;
+        ex |= z[h] + lg > s.mref[hb + h] + kTau;
       }
-      atomicMax(&s.mx[j & 1][hb + lane], mine);
-      named_bar_sync(1, kSoftThreads);
-      if ((warp & 3) == 0) {
-        const int hh = hb + lane;
-        const float mb = ord_float(s.mx[j & 1][hh]);
-        s.mx[(j + 1) & 1][hh] = kOrdMin;
-        const float old = s.mref[hh];
-        float f = 1.f;
-        if (mb > old + kTau) {
-          s.mref[hh] = mb;
-          f = exp2f(old - mb);  // 0 when old is -inf
-          if (j > 0) s.rescale[j & 1] = 1;
+      if (named_bar_or(1, kSoftThreads, ex)) {
+        // Slow path (always taken by the first block): block maximum per head
+        // across the 128 key lanes, raise the references that it exceeds.
+        int mine = kOrdMin;
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+          const int m = __reduce_max_sync(0xffffffffu, ord_int(z[h] + lg));
+          if (lane == h) mine = m;
         }
-        s.fac[hh] = f;
-        if (hh == 0) s.rescale[(j + 1) & 1] = 0;
-      }
-      named_bar_sync(1, kSoftThreads);
-      if (s.rescale[j & 1]) {
-        // O^T holds blocks < j: wait for the last PV, then scale each head's column.
-        w = mbar_wait(smem_u32(&s.bar_pv_done), (j - 1) & 1, p.err);
-        if (!named_bar_and(1, kSoftThreads, w)) { ok = false; break; }
-        tc_fence_after();
+        atomicMax(&s.mx[0][hb + lane], mine);
+        named_bar_sync(1, kSoftThreads);
+        if ((warp & 3) == 0) {
+          const int hh = hb + lane;
+          const float mb = ord_float(s.mx[0][hh]);
+          s.mx[0][hh] = kOrdMin;
+          const float old = s.mref[hh];
+          float f = 1.f;
+          if (mb > old + kTau) {
+            s.mref[hh] = mb;
+            f = exp2f(old - mb);  // 0 when old is -inf
+          }
+          s.fac[hh] = f;
+        }
+        named_bar_sync(1, kSoftThreads);
+        if (j > 0) {
+          // O^T holds blocks < j: wait for the last PV, then scale each head's column.
+          w = mbar_wait(smem_u32(&s.bar_pv_done), (j - 1) & 1, p.err);
+          if (!named_bar_and(1, kSoftThreads, w)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll 1
-        for (int tile = 0; tile < 4; ++tile) {
-          uint32_t v[32];
-          const uint32_t a = tmem + lane_base + tile * kNH + hb;
-          tmem_ld32(a, v);
-          tmem_wait_ld();
+          for (int tile = 0; tile < 4; ++tile) {
+            uint32_t v[32];
+            const uint32_t a = tmem + lane_base + tile * kNH + hb;
+            tmem_ld32(a, v);
+            tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 32; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * s.fac[hb + h]);
-          tmem_st32(a, v);
+            for (int h = 0; h < 32; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * s.fac[hb + h]);
+            tmem_st32(a, v);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+#pragma unroll
+          for (int h = 0; h < 32; ++h) lpart[h] *= s.fac[hb + h];
         }
-        tmem_wait_st();
-        tc_fence_before();
       }
-#pragma unroll
-      for (int h = 0; h < 32; ++h) lpart[h] *= s.fac[hb + h];
       // ---- P row r (this thread's 32 heads) and the row sums
       if (PP == 2 && KVP == 1 && j > 0) {
         // the single P-lo buffer is still read by PV of block j-1
@@ -350,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           const int h = c * 16 + k;
-          const float pw = exp2f(z[h] + lg - s.mref[hb + h]);   // 0 for invalid rows
+          const float pw = ex2_approx(z[h] + lg - s.mref[hb + h]);   // 0 for invalid rows
           x[k] = pw;
           lpart[h] += pw * isr;
         }
@@ -453,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
     }
   } else {
     // =================================================================== gather producers
-    const int pt = threadIdx.x - kProdWarp0 * 32;  // 0..95
+    const int pt = threadIdx.x - kProdWarp0 * 32;
     const uint32_t first = tok_idx[0];
     for (int j = 0; j < nblk; ++j) {
       const int slot = j % NST;
@@ -481,6 +496,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
       }
       named_bar_sync(2, kProdThreads);
       if (KVP == 1) {
+        // 128 rows x 36 chunks of 16 B, consecutive threads on consecutive
+        // chunks of a row, into the SW64 operand layout
 #pragma unroll 4
         for (int it = 0; it < kBK * 36 / kProdThreads; ++it) {
           const int i = it * kProdThreads + pt;
@@ -490,6 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
           cp_async16(dst, p.latent + static_cast<int64_t>(s.idx[row]) * kD + c * 16, 16);
         }
         cp_async_wait_all();
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&s.bar_kv_full[slot]));
       } else {
         for (int it = 0; it < kBK * 36 / kProdThreads; ++it) {
           const int i = it * kProdThreads + pt;
@@ -515,9 +534,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const Params p) {
           *reinterpret_cast<uint4*>(&s.kv[slot][0][off]) = hi;
           *reinterpret_cast<uint4*>(&s.kv[slot][KVP - 1][off]) = lo;
         }
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&s.bar_kv_full[slot]));
       }
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&s.bar_kv_full[slot]));
     }
   }
 
@@ -535,7 +554,7 @@ static smla_status_t launch_t(const Params& p, cudaStream_t stream) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return fail_cuda(e, "prefill smem attribute");
   dim3 grid(p.T, (p.H + kNH - 1) / kNH);
-  prefill_kernel<QP, KVP, PP, NST, SC><<<grid, kThreads, smem, stream>>>(p);
+  prefill_kernel<QP, KVP, PP, NST, SC><<<grid, threads_for(KVP), smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, "prefill launch");
   return SMLA_OK;

@@ -80,6 +80,16 @@ SMLA_DEVICE_INLINE void fence_proxy_async_smem() {
 SMLA_DEVICE_INLINE void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Named barrier that also ORs a predicate over the participating threads.
+SMLA_DEVICE_INLINE bool named_bar_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
 // Named barrier that also ANDs a predicate over the participating threads,
 // so that a give-up decision taken by any thread is taken by all of them.
 SMLA_DEVICE_INLINE bool named_bar_and(int id, int nthreads, bool pred) {
@@ -112,6 +122,17 @@ SMLA_DEVICE_INLINE void tma_load_2d(uint32_t dst, const CUtensorMap* m, int x, i
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
           dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Four rows (y0..y3) x one box of columns starting at x, gathered into four
+// consecutive box-rows of shared memory (tensor map box = [box_x, 1]).
+SMLA_DEVICE_INLINE void tma_gather4_2d(uint32_t dst, const CUtensorMap* m, int x, int y0, int y1, int y2, int y3,
+                                       uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
       : "memory");
 }
 
@@ -202,6 +223,29 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, int a_mn, in
 SMLA_DEVICE_INLINE uint16_t f32x2_to_e4m3x2(float a, float b) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(r) : "f"(a), "f"(b));
+  return r;
+}
+// 2^x with the hardware approximation (MUFU), flushing subnormal results.
+SMLA_DEVICE_INLINE float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+// Two floats -> packed half2 (round to nearest even), lo half = a.
+SMLA_DEVICE_INLINE uint32_t f32x2_to_f16x2(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(a), "f"(b));
+  return r;
+}
+// half2 -> two e4m3 bytes (round to nearest even, saturating).
+SMLA_DEVICE_INLINE uint16_t f16x2_to_e4m3x2(uint32_t v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(v));
+  return r;
+}
+SMLA_DEVICE_INLINE uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 // Two e4m3 bytes -> half2 (exact).

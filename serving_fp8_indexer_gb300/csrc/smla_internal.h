@@ -14,9 +14,10 @@ smla_status_t fail(smla_status_t st, const char* fmt, ...);
 smla_status_t fail_cuda(cudaError_t e, const char* what);
 
 // 2-D uint8 tensor map [rows][inner] (row pitch = inner bytes), box
-// [box_rows][box_inner], 128-byte swizzle, zero fill out of bounds.
+// [box_rows][box_inner], 128- (default) or 64-byte swizzle, zero fill out of
+// bounds.
 bool encode_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-                      uint32_t box_rows);
+                      uint32_t box_rows, int swizzle_bytes = 128);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
