@@ -14,7 +14,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libsmla.so")
 SOURCES = ["abi.cu", "indexer.cu", "topk.cu", "prefill.cu"]
-HEADERS = ["ptx.cuh", "smla_internal.h", "prefill_kernel.cuh"]
+HEADERS = ["ptx.cuh", "smla_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -69,7 +69,7 @@ constexpr int kProdWarp0 = 9;
 __host__ __device__ constexpr int prod_warps(int) { return 3; }
 __host__ __device__ constexpr int threads_for(int kvp) { return kSoftThreads + 32 + 32 * prod_warps(kvp); }
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 256;  // S^T columns [256, 320); O^T tiles at [0, 256)
+constexpr uint32_t kTmemS = 256;  // S^T accumulators (64 columns each) from 256; O^T tiles at [0, 256)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTau = 8.0f;      // lazy-rescale threshold (log2 units)
 constexpr int kOrdMin = static_cast<int>(0x80000000u);
@@ -292,6 +292,13 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         tmem_wait_ld();
 #pragma unroll
         for (int h = 0; h < 32; ++h) z[h] = __uint_as_float(v[h]);
+#pragma unroll
+        for (int a = 1; a < QP * KVP; ++a) {
+          tmem_ld32(tmem + lane_base + kTmemS + a * kNH + hb, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 32; ++h) z[h] += __uint_as_float(v[h]);
+        }
       }
       tc_fence_before();
       const bool valid = j * kBK + r < n;
@@ -418,53 +425,69 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     }
   } else if (warp == kMmaWarp) {
     // =================================================================== MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t IDESC_QK = idesc_e4m3_f32(kBK, kNH, 0, 0);
-      constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, kNH, 1, 1);
-      bool ok = mbar_wait(smem_u32(&s.bar_q), 0, p.err);
-      for (int j = 0; ok && j < nblk; ++j) {
-        const int slot = j % NST;
-        if (!mbar_wait(smem_u32(&s.bar_kv_full[slot]), (j / NST) & 1, p.err)) break;
-        tc_fence_after();
-        uint32_t acc = 0;
-#pragma unroll 1
-        for (int qp = 0; qp < QP; ++qp)
-#pragma unroll 1
-          for (int kp = 0; kp < KVP; ++kp)
+    // The whole warp runs the loop (operands stay warp-uniform); one elected
+    // lane issues the tcgen05 instructions and commits.
+    const bool leader = elect_one();
+    constexpr uint32_t IDESC_QK = idesc_e4m3_f32(kBK, kNH, 0, 0);
+    constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, kNH, 1, 1);
+    const uint64_t qk_b0 = make_sdesc(smem_u32(s.q[0]), 16, 512, kSwizzle64B);
+    const uint64_t kv_a0 = make_sdesc(smem_u32(s.kv[0][0]), 16, 512, kSwizzle64B);
+    const uint64_t pv_a0 = make_sdesc(smem_u32(s.kv[0][0]), kChunkBytes, 512, kSwizzle64B);
+    const uint64_t plo0 = make_sdesc(smem_u32(s.plo), kChunkBytes, 512, kSwizzle64B);
+    bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_q), 0, p.err));
+    for (int j = 0; ok && j < nblk; ++j) {
+      const int slot = j % NST;
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_kv_full[slot]), (j / NST) & 1, p.err))) break;
+      tc_fence_after();
+      // descriptor address fields are in 16-byte units: add offsets >> 4
+      const uint64_t slot_off = static_cast<uint64_t>((slot * KVP * kKVBytes) >> 4);
+      if (leader) {
+        // The QP x KVP products go to separate S accumulators (summed by the
+        // softmax) and are interleaved, so consecutive MMAs never wait on the
+        // same accumulator.
 #pragma unroll
-            for (int kc = 0; kc < kChunks; ++kc)
+        for (int kc = 0; kc < kChunks; ++kc)
 #pragma unroll
-              for (int kk = 0; kk < 2; ++kk) {
-                const uint64_t ad =
-                    make_sdesc(smem_u32(s.kv[slot][kp]) + kc * kChunkBytes + kk * 32, 16, 512, kSwizzle64B);
-                const uint64_t bd = make_sdesc(smem_u32(s.q[qp]) + kc * (kNH * 64) + kk * 32, 16, 512, kSwizzle64B);
-                mma_f8f6f4_ss(tmem + kTmemS, ad, bd, IDESC_QK, acc);
-                acc = 1;
+          for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+            for (int qp = 0; qp < QP; ++qp)
+#pragma unroll
+              for (int kp = 0; kp < KVP; ++kp) {
+                const uint64_t ad = kv_a0 + slot_off + static_cast<uint64_t>((kp * kKVBytes + kc * kChunkBytes + kk * 32) >> 4);
+                const uint64_t bd = qk_b0 + static_cast<uint64_t>((qp * kQBytes + kc * (kNH * 64) + kk * 32) >> 4);
+                mma_f8f6f4_ss(tmem + kTmemS + (qp * KVP + kp) * kNH, ad, bd, IDESC_QK, (kc | kk) ? 1u : 0u);
               }
         mma_commit(smem_u32(&s.bar_s_full));
-        if (!mbar_wait(smem_u32(&s.bar_p_full), j & 1, p.err)) break;
-        tc_fence_after();
-        const uint32_t p_hi = smem_u32(&s.kv[slot][0][kRope * kChunkBytes]);
-        const uint32_t p_lo = (KVP == 2) ? smem_u32(&s.kv[slot][KVP - 1][kRope * kChunkBytes]) : smem_u32(s.plo);
-#pragma unroll 1
-        for (int tile = 0; tile < 4; ++tile) {
-          uint32_t pacc = j > 0 ? 1u : 0u;
-#pragma unroll 1
-          for (int pp = 0; pp < PP; ++pp)
-#pragma unroll 1
-            for (int kp = 0; kp < KVP; ++kp)
+      }
+      __syncwarp();
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_p_full), j & 1, p.err))) break;
+      tc_fence_after();
+      if (leader) {
+        // P hi sits in the slot's rope chunk; P lo in the rope-lo chunk or its own buffer
 #pragma unroll
-              for (int ks = 0; ks < kBK / 32; ++ks) {
-                const uint64_t ad = make_sdesc(smem_u32(s.kv[slot][kp]) + (2 * tile) * kChunkBytes + ks * 32 * 64,
-                                               kChunkBytes, 512, kSwizzle64B);
-                const uint64_t bd = make_sdesc((pp == 0 ? p_hi : p_lo) + ks * 32 * 64, kChunkBytes, 512, kSwizzle64B);
+        for (int pp = 0; pp < PP; ++pp)
+#pragma unroll
+          for (int kp = 0; kp < KVP; ++kp)
+#pragma unroll
+            for (int ks = 0; ks < kBK / 32; ++ks)
+#pragma unroll
+              for (int tile = 0; tile < 4; ++tile) {
+                const uint32_t pacc = (j > 0 || pp > 0 || kp > 0 || ks > 0) ? 1u : 0u;
+                const uint64_t ad = pv_a0 + slot_off +
+                                    static_cast<uint64_t>((kp * kKVBytes + (2 * tile) * kChunkBytes + ks * 32 * 64) >> 4);
+                uint64_t bd;
+                if (pp == 0)
+                  bd = pv_a0 + slot_off + static_cast<uint64_t>((kRope * kChunkBytes + ks * 32 * 64) >> 4);
+                else if (KVP == 2)
+                  bd = pv_a0 + slot_off + static_cast<uint64_t>(((KVP - 1) * kKVBytes + kRope * kChunkBytes + ks * 32 * 64) >> 4);
+                else
+                  bd = plo0 + static_cast<uint64_t>((ks * 32 * 64) >> 4);
                 mma_f8f6f4_ss(tmem + tile * kNH, ad, bd, IDESC_PV, pacc);
-                pacc = 1;
               }
-        }
         mma_commit(smem_u32(&s.bar_kv_empty[slot]));
         mma_commit(smem_u32(&s.bar_pv_done));
       }
+      __syncwarp();
     }
   } else {
     // =================================================================== gather producers

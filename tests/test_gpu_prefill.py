@@ -54,27 +54,36 @@ def test_bf16_tensorwise_chunk_end_to_end():
     _end_to_end(wl.e2e_chunk(B=2, L=600, q_len=200, k=256, H=128, h_idx=64))
 
 
-@pytest.mark.parametrize("H", [16, 32, 192])
+@pytest.mark.parametrize("H", [16, 32, 192, 256])
 def test_head_counts(H):
     w = wl.build(f"h{H}", 40 + H, [70], [200], 64, topk=130, H=H, q_dtype=wl.Q_BF16, sbs=0, sample_indices=True)
     _sampled(w)
 
 
-def test_single_key_rows_are_exact():
+def test_pair_kernel_e4m3_and_tensorwise():
+    # H = 128 groups run on the cluster-pair kernel: e4m3 q, unit and row scales
+    for sbs, seed in ((0, 50), (576, 51)):
+        w = wl.build(f"pair_fp8_{sbs}", seed, [90, 40], [300, 40], 64, topk=200, H=128, q_dtype=wl.Q_E4M3,
+                     sbs=sbs, sample_indices=True)
+        _sampled(w)
+
+
+@pytest.mark.parametrize("H", [64, 128])
+def test_single_key_rows_are_exact(H):
     """topk_lengths == 1: the softmax weight is exactly 1 and the output is
     the selected row's first 512 values (exact in bf16)."""
-    w = wl.build("one", 3, [40], [40], 64, topk=4, H=64, q_dtype=wl.Q_BF16, sbs=0, sample_indices=True)
+    w = wl.build("one", 3, [40], [40], 64, topk=4, H=H, q_dtype=wl.Q_BF16, sbs=0, sample_indices=True)
     lens = np.ones(40, np.uint32)
     out = run_prefill(w, torch.from_numpy(w.indices).cuda(), torch.from_numpy(lens).cuda())
     import oracle
     for t in range(40):
         v = oracle.decode_e4m3(w.latent[w.indices[t, 0]])[:512]
-        assert np.array_equal(out[t].float().cpu().numpy(), np.broadcast_to(v, (64, 512)).astype(np.float32))
+        assert np.array_equal(out[t].float().cpu().numpy(), np.broadcast_to(v, (H, 512)).astype(np.float32))
 
 
 def test_zero_length_rows_and_wide_stride():
     """topk_lengths == 0 gives zeros; indices_stride wider than the lengths."""
-    w = wl.build("zero", 4, [50], [300], 64, topk=200, H=64, q_dtype=wl.Q_BF16, sbs=0, sample_indices=True)
+    w = wl.build("zero", 4, [50], [300], 64, topk=200, H=128, q_dtype=wl.Q_BF16, sbs=0, sample_indices=True)
     idx = np.full((50, 256), 0xFFFFFFFF, np.uint32)
     idx[:, :200] = w.indices
     lens = w.topk_lengths.copy()
