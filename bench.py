@@ -118,17 +118,23 @@ def keys_tok(w):
 
 
 CASES = {
-    # the benchmarked workload
-    "chunk": dict(),
+    # the benchmarked workload: the whole path on the end-to-end chunk
+    "chunk": ("e2e_chunk", dict()),
     # the same shapes with one sequence of 1024 new tokens (inputs still
     # larger than L2), for ncu captures
-    "chunk_small": dict(B=1, q_len=1024),
+    "chunk_small": ("e2e_chunk", dict(B=1, q_len=1024)),
+    # the other workloads, stage by stage
+    "tiny": ("tiny_prefill", dict()),
+    "mtp_decode": ("mtp_decode_indexer", dict()),
+    "dsv32": ("dsv32_prefill", dict()),
+    "blockwise": ("blockwise_fp8_prefill", dict()),
 }
 
 
 def make_workload(case="chunk"):
     from serving_fp8_indexer_gb300 import workloads as wl
-    return wl.e2e_chunk(**CASES[case])
+    fn, kw = CASES[case]
+    return getattr(wl, fn)(**kw)
 
 
 def cpu_cores():
@@ -204,13 +210,18 @@ def run_reference(args, rank, world):
 
 
 def config_dict(w, world):
-    B, q_len = w.seqs.B, int(w.seqs.cu_q[1])
-    return {"workload": f"end-to-end prefill chunk: {B} seqs x 8192 cached tokens, {q_len} new each "
-                        f"(the last {q_len} positions); indexer H_idx=64 fp8 -> causal top-2048 -> sparse MLA H=128, "
-                        "bf16 q, tensorwise e4m3 latent, v_depth 512",
-            "tokens": int(w.seqs.T), "H": w.H, "H_idx": w.h_idx, "topk": w.topk, "page_size": w.seqs.page_size,
-            "l2": "inputs larger than L2 (q 2.4 GB, scores 0.5 GB); the 38 MB latent pool is L2-resident by design",
-            "parallelism": f"replicas x{world}"}
+    d = {"workload": w.name, "tokens": int(w.seqs.T), "sequences": int(w.seqs.B),
+         "kv_len_max": int(w.seqs.kv_len.max()), "page_size": w.seqs.page_size, "parallelism": f"replicas x{world}"}
+    if w.h_idx:
+        d.update({"H_idx": w.h_idx, "topk": w.topk})
+    if w.H:
+        d.update({"H": w.H, "q": "bf16" if w.q_dtype == 0 else "e4m3",
+                  "scale_block_size": w.scale_block_size, "v_depth": 512,
+                  "indices": "from the indexer + top-k" if w.h_idx else f"sampled top-{w.topk}"})
+    big = w.H and w.seqs.T * w.H * 576 * (2 if w.q_dtype == 0 else 1) > (129 << 20)
+    d["l2"] = ("inputs larger than L2 (q, out); the latent pool is L2-resident by design" if big else
+               "small workload: inputs fit in L2 (launch/latency-bound case)")
+    return d
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -221,50 +232,73 @@ def run_ours(args, rank, world):
     from serving_fp8_indexer_gb300 import build as smla_build
     smla_build.build()
     import serving_fp8_indexer_gb300 as smla
+    from serving_fp8_indexer_gb300 import workloads as wl
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     w = make_workload(args.case)
     s = w.seqs
     T, H, k = s.T, w.H, w.topk
+    has_idx, has_attn = w.h_idx > 0, w.H > 0
     stride = int(s.kv_len.max() + 3) // 4 * 4
+    pos = wl.token_positions(s)
+    kt = float((pos + 1).sum())
 
     seqs = smla.Seqs.from_host(s, dev)
-    q_idx = torch.from_numpy(w.q_idx).to(dev)
-    q_scale = torch.from_numpy(w.q_scale).to(dev)
-    k_pool = torch.from_numpy(w.k_pool).to(dev)
-    k_scale = torch.from_numpy(w.k_scale).to(dev)
-    latent = torch.from_numpy(w.latent).to(dev)
-    scales = torch.from_numpy(w.scales).to(dev)
-    q_attn = torch.from_numpy(w.q_attn.view(np.int16)).view(torch.bfloat16).to(dev)
-    scores = torch.empty((T, stride), device=dev)
-    idx = torch.empty((T, k), dtype=torch.uint32, device=dev)
-    lens = torch.empty((T,), dtype=torch.uint32, device=dev)
-    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    t_in = {}
+    if has_idx:
+        t_in["q_idx"] = torch.from_numpy(w.q_idx).to(dev)
+        t_in["q_scale"] = torch.from_numpy(w.q_scale).to(dev)
+        k_pool = torch.from_numpy(w.k_pool).to(dev)
+        k_scale = torch.from_numpy(w.k_scale).to(dev)
+        scores = torch.empty((T, stride), device=dev)
+        idx = torch.empty((T, k), dtype=torch.uint32, device=dev)
+        lens = torch.empty((T,), dtype=torch.uint32, device=dev)
+    else:
+        idx = torch.from_numpy(w.indices).to(dev)
+        lens = torch.from_numpy(w.topk_lengths).to(dev)
+    if has_attn:
+        latent = torch.from_numpy(w.latent).to(dev)
+        scales = None if w.scales is None else torch.from_numpy(w.scales).to(dev)
+        if w.q_dtype == wl.Q_BF16:
+            t_in["q_attn"] = torch.from_numpy(w.q_attn.view(np.int16)).view(torch.bfloat16).to(dev)
+        else:
+            t_in["q_attn"] = torch.from_numpy(w.q_attn).to(dev)
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
+    n_kernels = (2 if has_idx else 0) + (1 if has_attn else 0)
 
     def step(ev=None):
+        i = 0
         if ev is not None:
             ev[0].record(stream)
-        smla.indexer_scores(q_idx, q_scale, k_pool, k_scale, seqs, scores)
-        if ev is not None:
-            ev[1].record(stream)
-        smla.topk(scores, seqs, k, idx, lens)
-        if ev is not None:
-            ev[2].record(stream)
-        smla.sparse_prefill(q_attn, latent, scales, w.scale_block_size, idx, lens, w.softmax_scale, out)
-        if ev is not None:
-            ev[3].record(stream)
+        if has_idx:
+            smla.indexer_scores(t_in["q_idx"], t_in["q_scale"], k_pool, k_scale, seqs, scores)
+            if ev is not None:
+                ev[1].record(stream)
+            smla.topk(scores, seqs, k, idx, lens)
+            if ev is not None:
+                ev[2].record(stream)
+        if has_attn:
+            smla.sparse_prefill(t_in["q_attn"], latent, scales, w.scale_block_size, idx, lens, w.softmax_scale, out)
+            if ev is not None:
+                ev[3].record(stream)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
     smla.check_device_errors()
+    attn_len = np.minimum(pos + 1, k) if has_idx else w.topk_lengths.astype(np.int64)
+    flops = sparse_flops(attn_len, H) if has_attn else 0.0
 
-    from serving_fp8_indexer_gb300 import workloads as wl
-    pos = wl.token_positions(s)
-    flops = sparse_flops(np.minimum(pos + 1, k), H)
-    kt = float((pos + 1).sum())
+    graph = None
+    if args.graph:
+        # launch-bound workloads: replay one step as a CUDA graph
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        graph.replay()
+        torch.cuda.synchronize(dev)
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", 0)))
@@ -277,7 +311,10 @@ def run_ours(args, rank, world):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        if graph is not None:
+            graph.replay()
+        else:
+            step(evs[i])
     e1.record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
@@ -286,30 +323,39 @@ def run_ours(args, rank, world):
     smla.check_device_errors()
 
     total_ms = e0.elapsed_time(e1)
-    idx_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    topk_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    attn_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    stage = {}
+    if graph is None:
+        if has_idx:
+            stage["indexer"] = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+            stage["topk"] = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+        if has_attn:
+            a = 2 if has_idx else 0
+            stage["sparse_mla"] = statistics.mean(e[a].elapsed_time(e[3]) for e in evs)
     if world > 1:
-        t = torch.tensor([total_ms, idx_ms, topk_ms, attn_ms], device=dev)
+        keys = sorted(stage)
+        t = torch.tensor([total_ms] + [stage[x] for x in keys], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, idx_ms, topk_ms, attn_ms = [float(x) for x in t.tolist()]
+        total_ms = float(t[0])
+        for i, x in enumerate(keys):
+            stage[x] = float(t[i + 1])
     ms_step = total_ms / args.steps
 
     # ---- end to end through the C ABI with host buffers (pinned), copies timed
     e2e = None
     if not args.no_e2e:
-        h_qidx = torch.from_numpy(w.q_idx).pin_memory()
-        h_qs = torch.from_numpy(w.q_scale).pin_memory()
-        h_q = torch.from_numpy(w.q_attn.view(np.int16)).view(torch.bfloat16).pin_memory()
-        h_out = torch.empty((T, H, 512), dtype=torch.bfloat16).pin_memory()
+        host = {name: (torch.from_numpy(w.q_attn.view(np.int16)).view(torch.bfloat16) if name == "q_attn" and
+                       w.q_dtype == wl.Q_BF16 else
+                       torch.from_numpy({"q_idx": w.q_idx, "q_scale": w.q_scale, "q_attn": w.q_attn}[name])).pin_memory()
+                for name in t_in}
+        h_out = (torch.empty((T, H, 512), dtype=torch.bfloat16) if has_attn else
+                 torch.empty((T, k), dtype=torch.int32)).pin_memory()
         n_e2e = max(1, min(args.steps, 5))
 
         def e2e_step():
-            q_idx.copy_(h_qidx, non_blocking=True)
-            q_scale.copy_(h_qs, non_blocking=True)
-            q_attn.copy_(h_q, non_blocking=True)
+            for name, ht in host.items():
+                t_in[name].copy_(ht, non_blocking=True)
             step()
-            h_out.copy_(out, non_blocking=True)
+            h_out.copy_(out if has_attn else idx.view(torch.int32), non_blocking=True)
 
         e2e_step()
         torch.cuda.synchronize(dev)
@@ -325,31 +371,36 @@ def run_ours(args, rank, world):
             t = torch.tensor([e2e_ms], device=dev)
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
             e2e_ms = float(t.item())
-        bi = h_qidx.numel() + h_qs.numel() * 4 + h_q.numel() * 2
-        bo = h_out.numel() * 2
-        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": int(bi),
-               "d2h_bytes_per_step": int(bo), "ms_per_step": e2e_ms}
+        bi = sum(ht.numel() * ht.element_size() for ht in host.values())
+        bo = h_out.numel() * h_out.element_size()
+        ev = world * (flops if has_attn else kt) / (e2e_ms * 1e-3)
+        e2e = {"value": ev / 1e12 if has_attn else ev, "unit": "TFLOP/s" if has_attn else "keys·tok/s",
+               "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo), "ms_per_step": e2e_ms}
 
     if rank != 0:
         return
     peaks, src = load_peaks()
     bf16_peak = peak_value(peaks, "bf16_tflops_sustained")
     hbm = peak_value(peaks, "hbm_gbs")
-    attn_tflops = flops / (attn_ms * 1e-3) / 1e12
-    frac = attn_tflops / bf16_peak
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        try:
-            traffic = json.load(open(prof)).get("prefill_kernel_bytes_per_launch")
-        except Exception:
-            traffic = None
-    idx_bytes = q_idx.numel() + q_scale.numel() * 4 + k_pool.numel() + k_scale.numel() * 4 + 4 * kt
-    topk_bytes = 4 * kt + 4 * T * k + 4 * T
+    stages = {}
+    if "indexer" in stage:
+        idx_bytes = w.q_idx.nbytes + w.q_scale.nbytes + w.k_pool.nbytes + w.k_scale.nbytes + 4 * kt
+        stages["indexer"] = {"ms": stage["indexer"], "TFLOP/s": 1e-12 * kt * w.h_idx * 256 / (stage["indexer"] * 1e-3),
+                             "GB/s_algorithmic": 1e-9 * idx_bytes / (stage["indexer"] * 1e-3)}
+        topk_bytes = 4 * kt + 4 * T * k + 4 * T
+        gbs = 1e-9 * topk_bytes / (stage["topk"] * 1e-3)
+        stages["topk"] = {"ms": stage["topk"], "GB/s_algorithmic": gbs, "frac_hbm": gbs / hbm}
+    if "sparse_mla" in stage:
+        tf = flops / (stage["sparse_mla"] * 1e-3) / 1e12
+        stages["sparse_mla"] = {"ms": stage["sparse_mla"], "TFLOP/s": tf, "frac_bf16_peak": tf / bf16_peak}
+    if has_attn:
+        value, unit = world * flops / (ms_step * 1e-3) / 1e12, "TFLOP/s"
+    else:
+        value, unit = world * kt / (ms_step * 1e-3), "keys·tok/s"
     line = {
         "metric": METRIC,
-        "value": world * flops / (ms_step * 1e-3) / 1e12,
-        "unit": "TFLOP/s",
+        "value": value,
+        "unit": unit,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -360,23 +411,28 @@ def run_ours(args, rank, world):
         "dtype": "e4m3 MMA (bf16 q and P as e4m3 hi+lo), f32 accumulate",
         "data": "synthetic",
         "config": config_dict(w, world),
-        "stages": {
-            "indexer": {"ms": idx_ms, "TFLOP/s": 1e-12 * kt * w.h_idx * 256 / (idx_ms * 1e-3),
-                        "GB/s_algorithmic": 1e-9 * idx_bytes / (idx_ms * 1e-3)},
-            "topk": {"ms": topk_ms, "GB/s_algorithmic": 1e-9 * topk_bytes / (topk_ms * 1e-3),
-                     "frac_hbm": 1e-9 * topk_bytes / (topk_ms * 1e-3) / hbm},
-            "sparse_mla": {"ms": attn_ms, "TFLOP/s": attn_tflops, "frac_bf16_peak": frac},
-        },
-        "indexer_topk": {"value": world * kt / ((idx_ms + topk_ms) * 1e-3), "unit": "keys·tok/s"},
-        "roofline": {"bound": "tensor", "kernel": "prefill_kernel (sparse MLA)", "achieved": attn_tflops,
-                     "peak": bf16_peak, "unit": "TFLOP/s", "frac": frac, "traffic": traffic,
-                     "peak_source": f"{src} bf16 dense (sustained)"},
-        "gpu_launches": 3 * args.steps,
+        "stages": stages,
+        "gpu_launches": n_kernels * args.steps,
         "clocks": clocks,
     }
+    if args.graph:
+        line["config"]["launch"] = "CUDA graph replay of one step"
+    if has_idx:
+        line["indexer_topk"] = {"value": world * kt / ((stage.get("indexer", ms_step) + stage.get("topk", 0.0)) * 1e-3),
+                                "unit": "keys·tok/s"}
+    if "sparse_mla" in stage:
+        tf = stages["sparse_mla"]["TFLOP/s"]
+        traffic = None
+        line["roofline"] = {"bound": "tensor", "kernel": "prefill_kernel (sparse MLA)", "achieved": tf,
+                            "peak": bf16_peak, "unit": "TFLOP/s", "frac": tf / bf16_peak, "traffic": traffic,
+                            "peak_source": f"{src} bf16 dense (sustained)"}
+    elif "topk" in stage:
+        line["roofline"] = {"bound": "hbm", "kernel": "topk_kernel", "achieved": stages["topk"]["GB/s_algorithmic"],
+                            "peak": hbm, "unit": "GB/s", "frac": stages["topk"]["frac_hbm"], "traffic": None,
+                            "peak_source": f"{src} HBM copy"}
     if e2e is not None:
         line["e2e"] = e2e
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and args.case == "chunk":
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line), flush=True)
 
@@ -390,6 +446,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", choices=sorted(CASES), default="chunk")
+    ap.add_argument("--graph", action="store_true", help="replay each step as a CUDA graph")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

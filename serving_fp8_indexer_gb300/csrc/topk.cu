@@ -7,11 +7,14 @@
 //   * one CTA per token; the token's valid scores (keys 0..pos) are read
 //     once from HBM (float4, coalesced) into shared memory as
 //     order-preserving 32-bit keys;
-//   * three histogram passes (11 + 11 + 10 bits, shared-memory atomics)
-//     pin the exact k-th largest key value;
-//   * one stable compaction pass in logical-key order emits every key above
-//     that value plus the lowest-keyed ties, mapped to physical rows through
-//     the page table.
+//   * the row's min/max (taken while loading) give the highest bit in which
+//     the keys differ; one 11-bit histogram pass over the row from there
+//     finds the bin holding the k-th largest, whose keys are then collected
+//     into a short candidate list where the remaining digits are resolved
+//     (the row is re-scanned only if that list overflows);
+//   * one stable compaction pass in logical-key order (warp ballots over
+//     warp-contiguous key ranges) emits every key above that value plus the
+//     lowest-keyed ties, mapped to physical rows through the page table.
 // Tokens with pos + 1 <= k take every valid key without selecting.
 #include <algorithm>
 
@@ -37,6 +40,8 @@ struct Params {
   uint32_t* indices;
   uint32_t* lens;
   int cache_cap;  // floats of the row cached in shared memory
+  int cand_cap;   // keys of the boundary bin kept in the candidate list
+  int pt_cap;     // page ids staged in shared memory
   unsigned* err;
 };
 
@@ -86,21 +91,54 @@ __device__ __forceinline__ uint32_t phys_row(const Params& p, int b, int key) {
   return static_cast<uint32_t>(pid) * static_cast<uint32_t>(p.page_size) + static_cast<uint32_t>(key % p.page_size);
 }
 
+// Finds the digit bin holding the krem-th largest candidate (bins counted
+// from the top), returns it and subtracts the count above it from krem.
+__device__ __forceinline__ int select_bin(const uint32_t* hist, int& krem, int* warp_tot, int* sh_bin,
+                                          int* sh_above) {
+  const int tid = threadIdx.x;
+  const int rt = kThreads - 1 - tid;  // thread rt owns bins [rt*4, rt*4+4)
+  int local = 0;
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) local += hist[rt * kBinsPerThread + j];
+  int total;
+  int c = block_exclusive_scan(local, warp_tot, &total);
+#pragma unroll
+  for (int j = kBinsPerThread - 1; j >= 0; --j) {
+    const int bin = rt * kBinsPerThread + j;
+    const int h = hist[bin];
+    if (c < krem && c + h >= krem) {
+      *sh_bin = bin;
+      *sh_above = c;
+    }
+    c += h;
+  }
+  __syncthreads();
+  const int bin = *sh_bin;
+  krem -= *sh_above;
+  __syncthreads();
+  return bin;
+}
+
 __global__ void __launch_bounds__(kThreads) topk_kernel(const Params p) {
-  extern __shared__ uint32_t cache[];
+  extern __shared__ uint32_t smem_dyn[];
+  uint32_t* cache = smem_dyn;                 // the row, as ordered keys
+  uint32_t* cand = smem_dyn + p.cache_cap;    // candidate list
+  int* ptab = reinterpret_cast<int*>(cand + p.cand_cap);  // page ids of the token's sequence
   __shared__ uint32_t hist[kBins];
   __shared__ int warp_tot[kWarps + 1];
-  __shared__ int sh_b, sh_bin, sh_above;
+  __shared__ uint32_t s_wmin[kWarps], s_wmax[kWarps];
+  __shared__ int sh_b, sh_bin, sh_above, s_ncand;
 
   const int t = blockIdx.x;
   const int tid = threadIdx.x;
-  if (tid == 0) {
-    int lo = 0, hi = p.B - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (p.cu_q[mid + 1] <= t) lo = mid + 1; else hi = mid;
+  if (tid < 32) {
+    // sequence of token t: the number of sequence ends cu_q[b+1] <= t
+    int cnt = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int bb = b0 + tid;
+      cnt += __popc(__ballot_sync(0xffffffffu, bb < p.B && p.cu_q[bb + 1] <= t));
     }
-    sh_b = lo;
+    if (tid == 0) sh_b = min(cnt, p.B - 1);
   }
   __syncthreads();
   const int b = sh_b;
@@ -121,8 +159,14 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const Params p) {
     return;
   }
 
+  // the sequence's page ids, for the logical -> physical row mapping
+  const int npages = min(p.max_pages, (n + p.page_size - 1) / p.page_size);
+  const bool pt_cached = npages <= p.pt_cap;
+  for (int i = tid; i < (pt_cached ? npages : 0); i += kThreads)
+    ptab[i] = p.page_table[static_cast<int64_t>(b) * p.max_pages + i];
   const float* row = p.scores + static_cast<int64_t>(t) * p.stride;
   const bool cached = n <= p.cache_cap;
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
   if (cached) {
     const int n4 = n >> 2;
     const float4* row4 = reinterpret_cast<const float4*>(row);
@@ -131,89 +175,152 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const Params p) {
       uint4 u;
       u.x = ordered(v.x); u.y = ordered(v.y); u.z = ordered(v.z); u.w = ordered(v.w);
       reinterpret_cast<uint4*>(cache)[i] = u;
+      kmin = min(kmin, min(min(u.x, u.y), min(u.z, u.w)));
+      kmax = max(kmax, max(max(u.x, u.y), max(u.z, u.w)));
     }
-    for (int i = (n4 << 2) + tid; i < n; i += kThreads) cache[i] = ordered(row[i]);
+    for (int i = (n4 << 2) + tid; i < n; i += kThreads) {
+      const uint32_t u = ordered(row[i]);
+      cache[i] = u;
+      kmin = min(kmin, u);
+      kmax = max(kmax, u);
+    }
+  } else {
+    for (int i = tid; i < n; i += kThreads) {
+      const uint32_t u = ordered(row[i]);
+      kmin = min(kmin, u);
+      kmax = max(kmax, u);
+    }
   }
   auto key_at = [&](int i) -> uint32_t { return cached ? cache[i] : ordered(row[i]); };
 
-  // ---- radix select of the k-th largest ordered key
-  uint32_t prefix = 0;
-  int krem = k;
-  const int shifts[3] = {21, 10, 0};
-  const int widths[3] = {11, 11, 10};
-#pragma unroll
-  for (int pass = 0; pass < 3; ++pass) {
-    const int sh = shifts[pass], wd = widths[pass];
-    const uint32_t mask = (1u << wd) - 1u;
-    for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
-    __syncthreads();
-    for (int i = tid; i < n; i += kThreads) {
-      const uint32_t u = key_at(i);
-      if (pass == 0 || (u >> (sh + wd)) == prefix) atomicAdd(&hist[(u >> sh) & mask], 1u);
-    }
-    __syncthreads();
-    // Count of elements in bins above each thread's bins: scan in reverse.
-    const int rt = kThreads - 1 - tid;  // thread rt owns bins [rt*4, rt*4+4)
-    int local = 0;
-#pragma unroll
-    for (int j = 0; j < kBinsPerThread; ++j) local += hist[rt * kBinsPerThread + j];
-    int total;
-    int above = block_exclusive_scan(local, warp_tot, &total);
-    int c = above;
-#pragma unroll
-    for (int j = kBinsPerThread - 1; j >= 0; --j) {
-      const int bin = rt * kBinsPerThread + j;
-      const int h = hist[bin];
-      if (c < krem && c + h >= krem) {
-        sh_bin = bin;
-        sh_above = c;
-      }
-      c += h;
-    }
-    __syncthreads();
-    prefix = (prefix << wd) | static_cast<uint32_t>(sh_bin);
-    krem -= sh_above;
-    __syncthreads();
+  // ---- exact k-th largest ordered key.  Bits above the highest bit in
+  // which the row's keys differ are common to every key, so the first
+  // 11-bit digit starts there.  One histogram pass over the row finds the
+  // digit bin holding the k-th largest; the keys of that bin are collected
+  // into a short candidate list on which the remaining digits are resolved.
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if ((tid & 31) == 0) {
+    s_wmin[tid >> 5] = kmin;
+    s_wmax[tid >> 5] = kmax;
   }
-  const uint32_t thr = prefix;  // exact k-th largest key; krem ties of it are taken
+  for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+  if (tid == 0) s_ncand = 0;
+  __syncthreads();
+  kmin = s_wmin[0];
+  kmax = s_wmax[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) {
+    kmin = min(kmin, s_wmin[w]);
+    kmax = max(kmax, s_wmax[w]);
+  }
+  const uint32_t diff = kmin ^ kmax;
+  int krem = k;
+  uint32_t thr = kmax;  // all keys equal: every key is a tie of kmax
+  if (diff != 0) {
+    int top = 31 - __clz(diff);
+    uint32_t hi_mask = top == 31 ? 0u : ~((2u << top) - 1u);
+    uint32_t hi_val = kmax & hi_mask;
+    // pass over the whole row
+    int sh = max(0, top - 10);
+    uint32_t dmask = (1u << (top - sh + 1)) - 1u;
+    for (int i = tid; i < n; i += kThreads) atomicAdd(&hist[(key_at(i) >> sh) & dmask], 1u);
+    __syncthreads();
+    int bin = select_bin(hist, krem, warp_tot, &sh_bin, &sh_above);
+    hi_val |= static_cast<uint32_t>(bin) << sh;
+    hi_mask |= dmask << sh;
+    top = sh - 1;
+    if (top >= 0) {
+      // candidates: the keys of the chosen bin (the same digit prefix)
+      const int ncand_cap = p.cand_cap;
+      for (int i = tid; i < n; i += kThreads) {
+        const uint32_t u = key_at(i);
+        if ((u & hi_mask) == hi_val) {
+          const int slot = atomicAdd(&s_ncand, 1);
+          if (slot < ncand_cap) cand[slot] = u;
+        }
+      }
+      __syncthreads();
+      const int nc = s_ncand;
+      const bool in_list = nc <= ncand_cap;
+      while (top >= 0) {
+        sh = max(0, top - 10);
+        dmask = (1u << (top - sh + 1)) - 1u;
+        for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+        __syncthreads();
+        if (in_list) {
+          for (int i = tid; i < nc; i += kThreads) {
+            const uint32_t u = cand[i];
+            if ((u & hi_mask) == hi_val) atomicAdd(&hist[(u >> sh) & dmask], 1u);
+          }
+        } else {
+          for (int i = tid; i < n; i += kThreads) {
+            const uint32_t u = key_at(i);
+            if ((u & hi_mask) == hi_val) atomicAdd(&hist[(u >> sh) & dmask], 1u);
+          }
+        }
+        __syncthreads();
+        bin = select_bin(hist, krem, warp_tot, &sh_bin, &sh_above);
+        hi_val |= static_cast<uint32_t>(bin) << sh;
+        hi_mask |= dmask << sh;
+        top = sh - 1;
+      }
+    }
+    thr = hi_val;
+  }
+  // thr = exact k-th largest key; krem of its ties are taken (lowest keys first)
 
-  // ---- stable compaction in logical-key order
-  int base = 0, tie_base = 0;
-  for (int start = 0; start < n; start += kThreads * 4) {
-    uint32_t u[4];
-    int neq = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = start + tid * 4 + j;
-      u[j] = i < n ? key_at(i) : 0u;
-      neq += (i < n && u[j] == thr) ? 1 : 0;
-    }
-    int eq_total;
-    int tie_rank = tie_base + block_exclusive_scan(neq, warp_tot, &eq_total);
-    bool sel[4];
-    int nsel = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int i = start + tid * 4 + j;
-      bool s = false;
-      if (i < n) {
-        if (u[j] > thr) s = true;
-        else if (u[j] == thr) { s = tie_rank < krem; ++tie_rank; }
+  // ---- stable compaction in logical-key order.  Warp w owns the keys
+  // [w*span, (w+1)*span); lane l reads key base + 32m + l (conflict-free),
+  // and warp ballots keep the output in key order.
+  __syncthreads();  // s_wmin / s_wmax are reused below
+  const int lane = tid & 31, warp = tid >> 5;
+  const int span = ((n + kWarps - 1) / kWarps + 31) & ~31;
+  const int w0 = min(n, warp * span), w1 = min(n, w0 + span);
+  int ngt = 0, neq = 0;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t u = i < w1 ? key_at(i) : 0u;
+    ngt += __popc(__ballot_sync(0xffffffffu, i < w1 && u > thr));
+    neq += __popc(__ballot_sync(0xffffffffu, i < w1 && u == thr));
+  }
+  if (lane == 0) {
+    s_wmin[warp] = static_cast<uint32_t>(ngt);
+    s_wmax[warp] = static_cast<uint32_t>(neq);
+  }
+  __syncthreads();
+  int sel_base = 0, tie_base = 0;
+  for (int w = 0; w < warp; ++w) {
+    const int g = static_cast<int>(s_wmin[w]), e = static_cast<int>(s_wmax[w]);
+    sel_base += g + max(0, min(e, krem - tie_base));
+    tie_base += e;
+  }
+  const uint32_t lt = (1u << lane) - 1u;
+  int pos = sel_base, tie = tie_base;
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const uint32_t u = i < w1 ? key_at(i) : 0u;
+    const bool gt = i < w1 && u > thr, eq = i < w1 && u == thr;
+    const uint32_t beq = __ballot_sync(0xffffffffu, eq);
+    const int my_tie = tie + __popc(beq & lt);
+    const bool sel = gt || (eq && my_tie < krem);
+    const uint32_t bsel = __ballot_sync(0xffffffffu, sel);
+    if (sel) {
+      const int o = pos + __popc(bsel & lt);
+      if (o < k) {
+        if (pt_cached) {
+          const int pid = ptab[i / p.page_size];
+          out[o] = pid >= 0 ? static_cast<uint32_t>(pid) * static_cast<uint32_t>(p.page_size) +
+                                  static_cast<uint32_t>(i % p.page_size)
+                            : phys_row(p, b, i);
+        } else {
+          out[o] = phys_row(p, b, i);
+        }
       }
-      sel[j] = s;
-      nsel += s ? 1 : 0;
+      else atomicOr(p.err, kErrShape);
     }
-    int sel_total;
-    int pos = base + block_exclusive_scan(nsel, warp_tot, &sel_total);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (sel[j]) {
-        if (pos < k) out[pos] = phys_row(p, b, start + tid * 4 + j);
-        else atomicOr(p.err, kErrShape);
-        ++pos;
-      }
-    base += sel_total;
-    tie_base += eq_total;
+    pos += __popc(bsel);
+    tie += __popc(beq);
   }
   if (tid == 0) p.lens[t] = static_cast<uint32_t>(k);
 }
@@ -226,13 +333,16 @@ smla_status_t launch_topk(const float* scores, int64_t score_stride, const smla_
   if (seqs.T == 0) return SMLA_OK;
   // Cache the whole row when it fits in 160 KB of shared memory; otherwise
   // every pass re-reads it (from L2).
-  const int64_t cap = std::min<int64_t>(score_stride, 40 * 1024);
-  const size_t smem = static_cast<size_t>((cap + 3) & ~int64_t(3)) * sizeof(uint32_t);
+  const int64_t cap = (std::min<int64_t>(score_stride, 40 * 1024) + 3) & ~int64_t(3);
+  const int64_t cand_cap = 2048;
+  const int64_t pt_cap = std::min<int64_t>(seqs.max_pages, 4096);
+  const size_t smem = static_cast<size_t>(cap + cand_cap + pt_cap) * sizeof(uint32_t);
   cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return fail_cuda(e, "topk smem attribute");
   Params p{scores, score_stride, seqs.cu_q, seqs.kv_len, seqs.page_table, seqs.B, seqs.max_pages,
-           seqs.page_size, seqs.T, k, indices, topk_lengths, static_cast<int>(cap), err};
+           seqs.page_size, seqs.T, k, indices, topk_lengths, static_cast<int>(cap), static_cast<int>(cand_cap),
+           static_cast<int>(pt_cap), err};
   topk_kernel<<<seqs.T, kThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, "topk launch");
