@@ -34,11 +34,20 @@
 // when a block exceeds it by more than 2^8 (lazy rescale), keeping P <= 256
 // inside the e4m3 range; raising it rescales O^T and the row sums.
 //
-// Pipeline: NST gather slots (2 when they fit in shared memory).  Block
-// j+1's rows are gathered while block j goes through QK, softmax and PV.
-// The rope chunk of a slot (columns 512..575) is dead once QK has read it,
-// so the block's P (hi term) is written there; only the bf16 path's P lo
-// term needs a buffer of its own.
+// Pipeline: NST gather slots (2 when they fit in shared memory).  PV runs
+// key-quarter by key-quarter (32 rows of the slot per step, the four O^T
+// tiles interleaved) and commits each quarter back to the gather, so the
+// rows of block j+NST start arriving while PV of block j is still running.
+// The MMA warp polls the barriers and issues whichever work is ready: QK of
+// block j+1 runs under the softmax of block j (S is loaded into registers
+// first and then released).  Each QK and PV is issued as one straight run
+// of MMAs (measured: splitting a block's QK into five separately issued
+// groups doubled its tensor-pipe time), and consecutive MMAs always target
+// different accumulators (QK rotates over three S^T accumulators, PV over
+// the four O^T tiles): an MMA waits for the previous one on the same
+// accumulator, which takes about three issue intervals.  The rope chunk of a slot (columns 512..575) is dead once QK
+// has read it, so the block's P (hi term) is written there; only the bf16
+// path's P lo term needs a buffer of its own, written last.
 //
 // Warp roles: warps 0-7 softmax / epilogue (lane quarter w%4, head half
 // w/4; thread = one key x 32 heads), warp 8 MMA issuer and TMEM owner,
@@ -61,6 +70,7 @@ constexpr int kQBytes = kChunks * kNH * 64;   // 36864
 constexpr int kKVBytes = kChunks * kBK * 64;  // 73728
 constexpr int kChunkBytes = kBK * 64;         // 8192: one 64-column chunk of a block
 constexpr int kRope = 8;                      // chunk index of columns 512..575
+constexpr int kRowQ = 4;                      // key quarters a slot is released in
 constexpr int kSoftWarps = 8;
 constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kMmaWarp = 8;
@@ -98,7 +108,7 @@ template <int QP, int KVP, int PP, int NST>
 struct Smem {
   uint8_t q[QP][kQBytes];
   uint8_t kv[NST][KVP][kKVBytes];
-  uint8_t plo[(PP == 2 && KVP == 1) ? kChunkBytes : 16];  // P lo when no rope-lo chunk holds it
+  uint8_t plo[PP == 2 ? kChunkBytes : 16];  // P lo term (bf16 path)
   uint32_t idx[kBK];
   float srow[NST][kBK];  // per-row scale (1 for unit)
   float cs[kNH];         // softmax_scale * log2(e) / 2^e_h
@@ -106,7 +116,8 @@ struct Smem {
   float fac[kNH];        // rescale factor of the current block; row sums at the end
   int mx[2][kNH];        // block maximum per head (order-preserving ints), by block parity
   int rescale[2];
-  unsigned long long bar_q, bar_kv_full[NST], bar_kv_empty[NST], bar_s_full, bar_p_full, bar_pv_done;
+  unsigned long long bar_q, bar_kv_full[NST], bar_kv_empty[NST][kRowQ];
+  unsigned long long bar_s_full, bar_s_free, bar_p_full, bar_pv_done;
   uint32_t tmem_base;
 };
 
@@ -145,12 +156,39 @@ __device__ __forceinline__ uint4 quant16(const float (&x)[16]) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Issues QK of one block: S^T[128 keys x 64 heads] over the 576 columns,
+// the MMAs rotating over NACC accumulators (MMA i of the block goes to
+// accumulator i % NACC; the first NACC overwrite).  Every operand offset is
+// a compile-time constant.
+template <int QP, int KVP, int NACC>
+__device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t a0, uint64_t b0, uint32_t idesc) {
+#pragma unroll
+  for (int kc = 0; kc < kChunks; ++kc)
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+      for (int qp = 0; qp < QP; ++qp)
+#pragma unroll
+        for (int kp = 0; kp < KVP; ++kp) {
+          const int i = ((kc * 2 + kk) * QP + qp) * KVP + kp;
+          // descriptor address fields are in 16-byte units: add offsets >> 4
+          const uint64_t ad = a0 + static_cast<uint64_t>((kp * kKVBytes + kc * kChunkBytes + kk * 32) >> 4);
+          const uint64_t bd = b0 + static_cast<uint64_t>((qp * kQBytes + kc * (kNH * 64) + kk * 32) >> 4);
+          mma_f8f6f4_ss(s_tmem + (i % NACC) * kNH, ad, bd, idesc, i < NACC ? 0u : 1u);
+        }
+}
+
 template <int QP, int KVP, int PP, int NST, int SC>
 __global__ void __launch_bounds__(threads_for(KVP), 1)
     prefill_kernel(const Params p) {
   using S = Smem<QP, KVP, PP, NST>;
+  static_assert(!(PP == 2 && KVP == 2), "P lo has a buffer only when rows are single-term");
+  // S^T accumulators: the block's QK MMAs rotate over three of them (summed
+  // by the softmax), because an MMA waits for the previous one on its
+  // accumulator (about three issue intervals) but not for other MMAs.
+  constexpr int kSAcc = 3;
   // per-lane partial row sums live in TMEM after the S accumulators
-  constexpr uint32_t kTmemL = kTmemS + kNH * QP * KVP;
+  constexpr uint32_t kTmemL = kTmemS + kNH * kSAcc;
   static_assert(kTmemL + kNH <= kTmemCols, "TMEM budget");
   constexpr int kThreads = threads_for(KVP);
   constexpr int kProdThreads = 32 * prod_warps(KVP);
@@ -184,9 +222,10 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     mbar_init(smem_u32(&s.bar_q), kSoftThreads);
     for (int i = 0; i < NST; ++i) {
       mbar_init(smem_u32(&s.bar_kv_full[i]), kProdThreads);
-      mbar_init(smem_u32(&s.bar_kv_empty[i]), 1);
+      for (int q = 0; q < kRowQ; ++q) mbar_init(smem_u32(&s.bar_kv_empty[i][q]), 1);
     }
     mbar_init(smem_u32(&s.bar_s_full), 1);
+    mbar_init(smem_u32(&s.bar_s_free), kSoftThreads);
     mbar_init(smem_u32(&s.bar_p_full), kSoftThreads);
     mbar_init(smem_u32(&s.bar_pv_done), 1);
     s.rescale[0] = s.rescale[1] = 0;
@@ -303,7 +342,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
 #pragma unroll
         for (int h = 0; h < 32; ++h) z[h] = __uint_as_float(v[h]);
 #pragma unroll
-        for (int a = 1; a < QP * KVP; ++a) {
+        for (int a = 1; a < kSAcc; ++a) {
           tmem_ld32(tmem + lane_base + kTmemS + a * kNH + hb, v);
           tmem_wait_ld();
 #pragma unroll
@@ -311,6 +350,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         }
       }
       tc_fence_before();
+      mbar_arrive(smem_u32(&s.bar_s_free));  // S may now be overwritten by QK of block j+1
       const bool valid = j * kBK + r < n;
       const float sr = SC == kUnit ? 1.f : s.srow[slot][r];
       const float lg = SC == kUnit ? 0.f : __log2f(sr);
@@ -375,14 +415,9 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         }
       }
       // ---- P row r (this thread's 32 heads) and the row sums
-      if (PP == 2 && KVP == 1 && j > 0) {
-        // the single P-lo buffer is still read by PV of block j-1
-        w = mbar_wait(smem_u32(&s.bar_pv_done), (j - 1) & 1, p.err);
-        if (!named_bar_and(1, kSoftThreads, w)) { ok = false; break; }
-      }
       const float isr = 1.f / sr;
       uint8_t* p_hi = &s.kv[slot][0][kRope * kChunkBytes];
-      uint8_t* p_lo = (KVP == 2) ? &s.kv[slot][KVP - 1][kRope * kChunkBytes] : s.plo;
+      uint4 lo_keep[2];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         float x[16];
@@ -400,13 +435,23 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         tmem_st16(la, lv);
         const int c4 = half * 2 + c;
         if (PP == 2) {
-          uint4 hi, lo;
-          split16(x, hi, lo);
+          uint4 hi;
+          split16(x, hi, lo_keep[c]);
           *reinterpret_cast<uint4*>(p_hi + r * 64 + sw64(r, c4)) = hi;
-          *reinterpret_cast<uint4*>(p_lo + r * 64 + sw64(r, c4)) = lo;
         } else {
           *reinterpret_cast<uint4*>(p_hi + r * 64 + sw64(r, c4)) = quant16(x);
         }
+      }
+      // PV of block j-1 must have completed: the single P-lo buffer is read by
+      // it, and P of block j is only published once the MMA warp has issued
+      // PV j-1 (so p_full never runs a phase ahead of its consumer).
+      if (j > 0) {
+        w = mbar_wait(smem_u32(&s.bar_pv_done), (j - 1) & 1, p.err);
+        if (!named_bar_and(1, kSoftThreads, w)) { ok = false; break; }
+      }
+      if (PP == 2) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) *reinterpret_cast<uint4*>(s.plo + r * 64 + sw64(r, half * 2 + c)) = lo_keep[c];
       }
       tmem_wait_st();
       fence_proxy_async_smem();
@@ -451,8 +496,11 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     }
   } else if (warp == kMmaWarp) {
     // =================================================================== MMA issuer
-    // The whole warp runs the loop (operands stay warp-uniform); one elected
-    // lane issues the tcgen05 instructions and commits.
+    // The whole warp runs the loop (decisions are lane 0's polls, broadcast);
+    // one elected lane issues the tcgen05 instructions and commits.  Work
+    // items: all of block vj's PV once its P is written (first: its commits
+    // return the slot to the gather), else all of block qj's QK once its rows
+    // have landed and the softmax of block qj-1 has released S.
     const bool leader = elect_one();
     constexpr uint32_t IDESC_QK = idesc_e4m3_f32(kBK, kNH, 0, 0);
     constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, kNH, 1, 1);
@@ -461,57 +509,72 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     const uint64_t pv_a0 = make_sdesc(smem_u32(s.kv[0][0]), kChunkBytes, 512, kSwizzle64B);
     const uint64_t plo0 = make_sdesc(smem_u32(s.plo), kChunkBytes, 512, kSwizzle64B);
     bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_q), 0, p.err));
-    for (int j = 0; ok && j < nblk; ++j) {
-      const int slot = j % NST;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_kv_full[slot]), (j / NST) & 1, p.err))) break;
-      tc_fence_after();
-      // descriptor address fields are in 16-byte units: add offsets >> 4
-      const uint64_t slot_off = static_cast<uint64_t>((slot * KVP * kKVBytes) >> 4);
-      if (leader) {
-        // The QP x KVP products go to separate S accumulators (summed by the
-        // softmax) and are interleaved, so consecutive MMAs never wait on the
-        // same accumulator.
-#pragma unroll
-        for (int kc = 0; kc < kChunks; ++kc)
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-            for (int qp = 0; qp < QP; ++qp)
-#pragma unroll
-              for (int kp = 0; kp < KVP; ++kp) {
-                const uint64_t ad = kv_a0 + slot_off + static_cast<uint64_t>((kp * kKVBytes + kc * kChunkBytes + kk * 32) >> 4);
-                const uint64_t bd = qk_b0 + static_cast<uint64_t>((qp * kQBytes + kc * (kNH * 64) + kk * 32) >> 4);
-                mma_f8f6f4_ss(tmem + kTmemS + (qp * KVP + kp) * kNH, ad, bd, IDESC_QK, (kc | kk) ? 1u : 0u);
-              }
-        mma_commit(smem_u32(&s.bar_s_full));
+    int qj = 0;            // next QK block
+    int vj = 0;            // next PV block
+    bool s_free = true;    // S may be written by QK of block qj
+    unsigned long long t_idle = 0;
+    while (ok && vj < nblk) {
+      int act = 0;
+      if (lane == 0) {
+        if (vj < qj && mbar_test(smem_u32(&s.bar_p_full), vj & 1)) {
+          act = 2;
+        } else if (qj < nblk) {
+          if (!s_free) s_free = mbar_test(smem_u32(&s.bar_s_free), (qj - 1) & 1);
+          if (s_free && mbar_test(smem_u32(&s.bar_kv_full[qj % NST]), (qj / NST) & 1)) act = 1;
+        }
+        if (act == 0) {
+          const unsigned long long now = global_timer_ns();
+          if (t_idle == 0) t_idle = now;
+          else if (now - t_idle > kWaitLimitNs) {
+            atomicOr(p.err, kErrTimeout);
+            act = -1;
+          }
+        } else {
+          t_idle = 0;
+        }
       }
-      __syncwarp();
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_p_full), j & 1, p.err))) break;
+      act = __shfl_sync(0xffffffffu, act, 0);
+      if (act < 0) break;
+      if (act == 0) continue;
+      // both follow other threads' tcgen05 operations: the softmax's load of S
+      // (QK) or its TMEM rescale of O^T (PV)
       tc_fence_after();
-      if (leader) {
-        // P hi sits in the slot's rope chunk; P lo in the rope-lo chunk or its own buffer
+      if (act == 2) {
+        // O^T[512 vcols x 64 heads] += V^T P^T over the block's 128 keys, one
+        // 32-key quarter at a time with the four 128-column tiles interleaved;
+        // each quarter's rows go back to the gather when its MMAs complete.
+        // P hi sits in the slot's rope chunk, P lo in its own buffer.
+        const int slot = vj % NST;
+        const uint64_t slot_off = static_cast<uint64_t>((slot * KVP * kKVBytes) >> 4);
+        if (leader) {
 #pragma unroll
-        for (int pp = 0; pp < PP; ++pp)
+          for (int ks = 0; ks < kRowQ; ++ks) {
 #pragma unroll
-          for (int kp = 0; kp < KVP; ++kp)
+            for (int pp = 0; pp < PP; ++pp)
 #pragma unroll
-            for (int ks = 0; ks < kBK / 32; ++ks)
+              for (int kp = 0; kp < KVP; ++kp)
 #pragma unroll
-              for (int tile = 0; tile < 4; ++tile) {
-                const uint32_t pacc = (j > 0 || pp > 0 || kp > 0 || ks > 0) ? 1u : 0u;
-                const uint64_t ad = pv_a0 + slot_off +
-                                    static_cast<uint64_t>((kp * kKVBytes + (2 * tile) * kChunkBytes + ks * 32 * 64) >> 4);
-                uint64_t bd;
-                if (pp == 0)
-                  bd = pv_a0 + slot_off + static_cast<uint64_t>((kRope * kChunkBytes + ks * 32 * 64) >> 4);
-                else if (KVP == 2)
-                  bd = pv_a0 + slot_off + static_cast<uint64_t>(((KVP - 1) * kKVBytes + kRope * kChunkBytes + ks * 32 * 64) >> 4);
-                else
-                  bd = plo0 + static_cast<uint64_t>((ks * 32 * 64) >> 4);
-                mma_f8f6f4_ss(tmem + tile * kNH, ad, bd, IDESC_PV, pacc);
-              }
-        mma_commit(smem_u32(&s.bar_kv_empty[slot]));
-        mma_commit(smem_u32(&s.bar_pv_done));
+                for (int tile = 0; tile < 4; ++tile) {
+                  const uint32_t pacc = (vj > 0 || pp > 0 || kp > 0 || ks > 0) ? 1u : 0u;
+                  const uint64_t ad = pv_a0 + slot_off +
+                                      static_cast<uint64_t>((kp * kKVBytes + (2 * tile) * kChunkBytes + ks * 32 * 64) >> 4);
+                  const uint64_t bd = pp == 0 ? pv_a0 + slot_off + static_cast<uint64_t>((kRope * kChunkBytes + ks * 32 * 64) >> 4)
+                                              : plo0 + static_cast<uint64_t>((ks * 32 * 64) >> 4);
+                  mma_f8f6f4_ss(tmem + tile * kNH, ad, bd, IDESC_PV, pacc);
+                }
+            mma_commit(smem_u32(&s.bar_kv_empty[slot][ks]));
+          }
+          mma_commit(smem_u32(&s.bar_pv_done));
+        }
+        ++vj;
+      } else {
+        const uint64_t slot_off = static_cast<uint64_t>(((qj % NST) * KVP * kKVBytes) >> 4);
+        if (leader) {
+          issue_qk<QP, KVP, kSAcc>(tmem + kTmemS, kv_a0 + slot_off, qk_b0, IDESC_QK);
+          mma_commit(smem_u32(&s.bar_s_full));
+        }
+        ++qj;
+        s_free = false;
       }
       __syncwarp();
     }
@@ -520,10 +583,12 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     const int pt = threadIdx.x - kProdWarp0 * 32;
     const uint32_t first = tok_idx[0];
     const uint64_t keep = make_policy_evict_last();  // the latent pool stays in L2 over the q / out streams
+    bool ok = true;
     for (int j = 0; j < nblk; ++j) {
       const int slot = j % NST;
-      const bool w = mbar_wait(smem_u32(&s.bar_kv_empty[slot]), ((j / NST) & 1) ^ 1, p.err);
-      if (!named_bar_and(2, kProdThreads, w)) break;
+      const uint32_t par = ((j / NST) & 1) ^ 1;
+      const bool w = mbar_wait(smem_u32(&s.bar_kv_empty[slot][0]), par, p.err);
+      if (!named_bar_and(2, kProdThreads, ok && w)) break;
       // rows of this block: physical row and scale
       for (int rr = pt; rr < kBK; rr += kProdThreads) {
         const int key = j * kBK + rr;
@@ -545,49 +610,54 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         s.srow[slot][rr] = sr;
       }
       named_bar_sync(2, kProdThreads);
-      if (KVP == 1) {
-        // 128 rows x 36 chunks of 16 B, consecutive threads on consecutive
-        // chunks of a row, into the SW64 operand layout
+      // Key quarter q (rows 32q..32q+31) is refilled once PV of block j-NST
+      // has finished with it.
+      for (int q = 0; q < kRowQ; ++q) {
+        if (q > 0 && ok) ok = mbar_wait(smem_u32(&s.bar_kv_empty[slot][q]), par, p.err);
+        if (!ok) continue;
+        if (KVP == 1) {
+          // 32 rows x 36 16-byte pieces, consecutive threads on consecutive
+          // pieces of a row, into the SW64 operand layout
 #pragma unroll 4
-        for (int i = pt; i < kBK * 36; i += kProdThreads) {
-          const int row = i / 36, c = i - row * 36;
-          const int kc = c >> 2, c4 = c & 3;
-          const uint32_t dst = smem_u32(s.kv[slot][0]) + kc * kChunkBytes + row * 64 + sw64(row, c4);
-          cp_async16_hint(dst, p.latent + static_cast<int64_t>(s.idx[row]) * kD + c * 16, keep);
-        }
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&s.bar_kv_full[slot]));
-      } else {
-        for (int i = pt; i < kBK * 36; i += kProdThreads) {
-          const int row = i / 36, c = i - row * 36;
-          const int kc = c >> 2, c4 = c & 3;
-          const uint32_t rr = s.idx[row];
-          uint4 raw;
-          asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                       : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
-                       : "l"(p.latent + static_cast<int64_t>(rr) * kD + c * 16), "l"(keep));
-          const float ratio = p.scales[static_cast<int64_t>(rr) * p.nscale + (c >> 1)] / s.srow[slot][row];
-          const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-          float x[16];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 a = e4m3x2_to_f32x2(static_cast<uint16_t>(wv[k] & 0xffffu));
-            const float2 b = e4m3x2_to_f32x2(static_cast<uint16_t>(wv[k] >> 16));
-            x[4 * k + 0] = a.x * ratio;
-            x[4 * k + 1] = a.y * ratio;
-            x[4 * k + 2] = b.x * ratio;
-            x[4 * k + 3] = b.y * ratio;
+          for (int i = pt; i < 32 * 36; i += kProdThreads) {
+            const int row = 32 * q + i / 36, c = i % 36;
+            const int kc = c >> 2, c4 = c & 3;
+            const uint32_t dst = smem_u32(s.kv[slot][0]) + kc * kChunkBytes + row * 64 + sw64(row, c4);
+            cp_async16_hint(dst, p.latent + static_cast<int64_t>(s.idx[row]) * kD + c * 16, keep);
           }
-          uint4 hi, lo;
-          split16(x, hi, lo);
-          const uint32_t off = kc * kChunkBytes + row * 64 + sw64(row, c4);
-          *reinterpret_cast<uint4*>(&s.kv[slot][0][off]) = hi;
-          *reinterpret_cast<uint4*>(&s.kv[slot][KVP - 1][off]) = lo;
+        } else {
+          // blockwise rows: register dequantisation to x * s_blk / s_row, e4m3 hi + lo
+          for (int i = pt; i < 32 * 36; i += kProdThreads) {
+            const int row = 32 * q + i / 36, c = i % 36;
+            const int kc = c >> 2, c4 = c & 3;
+            const uint32_t rr = s.idx[row];
+            uint4 raw;
+            asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                         : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
+                         : "l"(p.latent + static_cast<int64_t>(rr) * kD + c * 16), "l"(keep));
+            const float ratio = p.scales[static_cast<int64_t>(rr) * p.nscale + (c >> 1)] / s.srow[slot][row];
+            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+            float x[16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 a = e4m3x2_to_f32x2(static_cast<uint16_t>(wv[k] & 0xffffu));
+              const float2 b = e4m3x2_to_f32x2(static_cast<uint16_t>(wv[k] >> 16));
+              x[4 * k + 0] = a.x * ratio;
+              x[4 * k + 1] = a.y * ratio;
+              x[4 * k + 2] = b.x * ratio;
+              x[4 * k + 3] = b.y * ratio;
+            }
+            uint4 hi, lo;
+            split16(x, hi, lo);
+            const uint32_t off = kc * kChunkBytes + row * 64 + sw64(row, c4);
+            *reinterpret_cast<uint4*>(&s.kv[slot][0][off]) = hi;
+            *reinterpret_cast<uint4*>(&s.kv[slot][KVP - 1][off]) = lo;
+          }
         }
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&s.bar_kv_full[slot]));
       }
+      if (KVP == 1) cp_async_wait_all();
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&s.bar_kv_full[slot]));
     }
   }
 

@@ -58,6 +58,16 @@ SMLA_DEVICE_INLINE bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of the phase with the given parity.
+SMLA_DEVICE_INLINE bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Waits for the phase with the given parity to complete.  Gives up after
 // kWaitLimitNs, records kErrTimeout and returns false.
 SMLA_DEVICE_INLINE bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
@@ -132,6 +142,11 @@ SMLA_DEVICE_INLINE uint64_t make_policy_evict_last() {
 SMLA_DEVICE_INLINE uint4 ld_stream16(const void* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }
 SMLA_DEVICE_INLINE void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 SMLA_DEVICE_INLINE void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Waits until at most N of this thread's committed cp.async groups are pending.
+template <int N>
+SMLA_DEVICE_INLINE void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // ------------------------------------------------------------------ TMA
 SMLA_DEVICE_INLINE void tma_prefetch_desc(const CUtensorMap* m) {
