@@ -34,25 +34,25 @@
 // when a block exceeds it by more than 2^8 (lazy rescale), keeping P <= 256
 // inside the e4m3 range; raising it rescales O^T and the row sums.
 //
-// Pipeline: NST gather slots (2 when they fit in shared memory).  PV runs
-// key-quarter by key-quarter (32 rows of the slot per step, the four O^T
-// tiles interleaved) and commits each quarter back to the gather, so the
+// Pipeline: NST gather slots (2 when they fit in shared memory).  The
+// producers fetch the next block's row indices and scales while the current
+// block's rows are in flight, so a slot refill starts with its copies.  PV
+// runs key-quarter by key-quarter (32 rows of the slot per step, the four
+// O^T tiles interleaved) and commits each quarter back to the gather, so the
 // rows of block j+NST start arriving while PV of block j is still running.
-// The MMA warp polls the barriers and issues whichever work is ready: QK of
-// block j+1 runs under the softmax of block j (S is loaded into registers
-// first and then released).  Each QK and PV is issued as one straight run
-// of MMAs (measured: splitting a block's QK into five separately issued
-// groups doubled its tensor-pipe time), and consecutive MMAs always target
-// different accumulators (QK rotates over three S^T accumulators, PV over
-// the four O^T tiles): an MMA waits for the previous one on the same
-// accumulator, which takes about three issue intervals.  The rope chunk of a slot (columns 512..575) is dead once QK
-// has read it, so the block's P (hi term) is written there; only the bf16
-// path's P lo term needs a buffer of its own, written last.
+// QK and PV have an issuing warp each: QK of block j+1 runs under the
+// softmax of block j (S is loaded into registers first and then released),
+// and PV of block j never queues behind the issue of QK j+1.  Each QK and PV
+// is issued as one straight run of MMAs (measured: splitting a block's QK
+// into five separately issued groups doubled its tensor-pipe time), and
+// consecutive MMAs always target different accumulators (QK alternates two
+// S^T accumulators, PV rotates over the four O^T tiles): an MMA waits for
+// the previous one on the same accumulator.
 //
-// Warp roles: warps 0-7 softmax / epilogue (lane quarter w%4, head half
-// w/4; thread = one key x 32 heads), warp 8 MMA issuer and TMEM owner,
-// warps 9-11 gather producers (cp.async 16 B into the SW64 layout, or a
-// register dequantisation of blockwise rows).
+// Warp roles (24 warps): warps 0-7 softmax / epilogue (lane quarter w%4,
+// head half w/4; thread = one key x 32 heads), warp 8 QK issuer and TMEM
+// owner, warp 9 PV issuer, warps 10-23 gather producers (cp.async 16 B into
+// the SW64 layout, or a register dequantisation of blockwise rows).
 #include <algorithm>
 
 #include "ptx.cuh"
@@ -73,14 +73,22 @@ constexpr int kRope = 8;                      // chunk index of columns 512..575
 constexpr int kRowQ = 4;                      // key quarters a slot is released in
 constexpr int kSoftWarps = 8;
 constexpr int kSoftThreads = kSoftWarps * 32;
-constexpr int kMmaWarp = 8;
-constexpr int kProdWarp0 = 9;
-// Producer warps: the gather is bound by the requests each warp keeps in
-// flight, so more warps gather faster (measured: 3 -> 8 warps doubles the
-// L2 -> SM rate of this access pattern).  Sixteen warps in all keep 128
-// registers per thread.
-__host__ __device__ constexpr int prod_warps(int) { return 7; }
-__host__ __device__ constexpr int threads_for(int kvp) { return kSoftThreads + 32 + 32 * prod_warps(kvp); }
+constexpr int kMmaWarp = 8;   // QK issuer, TMEM owner
+constexpr int kPvWarp = 9;    // PV issuer
+constexpr int kProdWarp0 = 10;
+// Producer warps: the gather is bound by the requests kept in flight, so
+// more warps gather faster (measured on this access pattern: 7 warps ~4.9,
+// 16 warps ~7.4 TB/s from L2).  24 warps in all launch with 80 registers a
+// thread; the softmax warpgroups then raise theirs to kSoftRegs and the
+// others drop to kLowRegs (setmaxnreg), within the launch allocation.
+__host__ __device__ constexpr int prod_warps(int) { return 14; }
+__host__ __device__ constexpr int threads_for(int kvp) { return kSoftThreads + 64 + 32 * prod_warps(kvp); }
+constexpr int kLaunchRegs = 80;
+constexpr int kSoftRegs = 152;
+constexpr int kLowRegs = 40;
+static_assert(kSoftThreads * kSoftRegs + (threads_for(1) - kSoftThreads) * kLowRegs <= threads_for(1) * kLaunchRegs,
+              "register split exceeds the launch allocation");
+static_assert(kSoftWarps % 4 == 0 && kMmaWarp % 4 == 0, "roles must split on warpgroup boundaries");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 256;  // S^T accumulators (64 columns each) from 256; O^T tiles at [0, 256)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -183,10 +191,11 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     prefill_kernel(const Params p) {
   using S = Smem<QP, KVP, PP, NST>;
   static_assert(!(PP == 2 && KVP == 2), "P lo has a buffer only when rows are single-term");
-  // S^T accumulators: the block's QK MMAs rotate over three of them (summed
-  // by the softmax), because an MMA waits for the previous one on its
-  // accumulator (about three issue intervals) but not for other MMAs.
-  constexpr int kSAcc = 3;
+  // S^T accumulators: the block's QK MMAs alternate between two of them
+  // (summed by the softmax), because an MMA waits for the previous one on
+  // its accumulator but not for other MMAs (measured: two alternating
+  // accumulators already run a block's QK as fast as three).
+  constexpr int kSAcc = 2;
   // per-lane partial row sums live in TMEM after the S accumulators
   constexpr uint32_t kTmemL = kTmemS + kNH * kSAcc;
   static_assert(kTmemL + kNH <= kTmemCols, "TMEM budget");
@@ -243,6 +252,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
 
   if (warp < kSoftWarps) {
     // =================================================================== softmax / epilogue
+    setmaxnreg_inc<kSoftRegs>();
     const int r = threadIdx.x & 127;        // key lane = TMEM lane
     const int half = warp >> 2;             // heads [32*half, 32*half + 32)
     const int hb = half * 32;
@@ -495,119 +505,109 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
       }
     }
   } else if (warp == kMmaWarp) {
-    // =================================================================== MMA issuer
-    // The whole warp runs the loop (decisions are lane 0's polls, broadcast);
-    // one elected lane issues the tcgen05 instructions and commits.  Work
-    // items: all of block vj's PV once its P is written (first: its commits
-    // return the slot to the gather), else all of block qj's QK once its rows
-    // have landed and the softmax of block qj-1 has released S.
+    // =================================================================== QK issuer
+    // QK of block j once its rows have landed and the softmax of block j-1
+    // has released S.  The whole warp runs the loop; one elected lane issues.
+    setmaxnreg_dec<kLowRegs>();
     const bool leader = elect_one();
     constexpr uint32_t IDESC_QK = idesc_e4m3_f32(kBK, kNH, 0, 0);
-    constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, kNH, 1, 1);
     const uint64_t qk_b0 = make_sdesc(smem_u32(s.q[0]), 16, 512, kSwizzle64B);
     const uint64_t kv_a0 = make_sdesc(smem_u32(s.kv[0][0]), 16, 512, kSwizzle64B);
+    bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_q), 0, p.err));
+    for (int j = 0; ok && j < nblk; ++j) {
+      const bool w = (j == 0 || mbar_wait(smem_u32(&s.bar_s_free), (j - 1) & 1, p.err)) &&
+                     mbar_wait(smem_u32(&s.bar_kv_full[j % NST]), (j / NST) & 1, p.err);
+      if (!__all_sync(0xffffffffu, w)) break;
+      tc_fence_after();  // after the softmax's tcgen05.ld of S
+      const uint64_t slot_off = static_cast<uint64_t>(((j % NST) * KVP * kKVBytes) >> 4);
+      if (leader) {
+        issue_qk<QP, KVP, kSAcc>(tmem + kTmemS, kv_a0 + slot_off, qk_b0, IDESC_QK);
+        mma_commit(smem_u32(&s.bar_s_full));
+      }
+      __syncwarp();
+    }
+  } else if (warp == kPvWarp) {
+    // =================================================================== PV issuer
+    // PV of block j once its P is written.  A warp of its own, so that PV is
+    // never queued behind the issue of the next block's QK.
+    setmaxnreg_dec<kLowRegs>();
+    const bool leader = elect_one();
+    constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, kNH, 1, 1);
     const uint64_t pv_a0 = make_sdesc(smem_u32(s.kv[0][0]), kChunkBytes, 512, kSwizzle64B);
     const uint64_t plo0 = make_sdesc(smem_u32(s.plo), kChunkBytes, 512, kSwizzle64B);
-    bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_q), 0, p.err));
-    int qj = 0;            // next QK block
-    int vj = 0;            // next PV block
-    bool s_free = true;    // S may be written by QK of block qj
-    unsigned long long t_idle = 0;
-    while (ok && vj < nblk) {
-      int act = 0;
-      if (lane == 0) {
-        if (vj < qj && mbar_test(smem_u32(&s.bar_p_full), vj & 1)) {
-          act = 2;
-        } else if (qj < nblk) {
-          if (!s_free) s_free = mbar_test(smem_u32(&s.bar_s_free), (qj - 1) & 1);
-          if (s_free && mbar_test(smem_u32(&s.bar_kv_full[qj % NST]), (qj / NST) & 1)) act = 1;
-        }
-        if (act == 0) {
-          const unsigned long long now = global_timer_ns();
-          if (t_idle == 0) t_idle = now;
-          else if (now - t_idle > kWaitLimitNs) {
-            atomicOr(p.err, kErrTimeout);
-            act = -1;
-          }
-        } else {
-          t_idle = 0;
-        }
-      }
-      act = __shfl_sync(0xffffffffu, act, 0);
-      if (act < 0) break;
-      if (act == 0) continue;
-      // both follow other threads' tcgen05 operations: the softmax's load of S
-      // (QK) or its TMEM rescale of O^T (PV)
-      tc_fence_after();
-      if (act == 2) {
-        // O^T[512 vcols x 64 heads] += V^T P^T over the block's 128 keys, one
-        // 32-key quarter at a time with the four 128-column tiles interleaved;
-        // each quarter's rows go back to the gather when its MMAs complete.
-        // P hi sits in the slot's rope chunk, P lo in its own buffer.
-        const int slot = vj % NST;
-        const uint64_t slot_off = static_cast<uint64_t>((slot * KVP * kKVBytes) >> 4);
-        if (leader) {
+    for (int j = 0; j < nblk; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_p_full), j & 1, p.err))) break;
+      tc_fence_after();  // after the softmax's TMEM rescale of O^T
+      // O^T[512 vcols x 64 heads] += V^T P^T over the block's 128 keys, one
+      // 32-key quarter at a time with the four 128-column tiles interleaved;
+      // each quarter's rows go back to the gather when its MMAs complete.
+      // P hi sits in the slot's rope chunk, P lo in its own buffer.
+      const int slot = j % NST;
+      const uint64_t slot_off = static_cast<uint64_t>((slot * KVP * kKVBytes) >> 4);
+      if (leader) {
 #pragma unroll
-          for (int ks = 0; ks < kRowQ; ++ks) {
+        for (int ks = 0; ks < kRowQ; ++ks) {
 #pragma unroll
-            for (int pp = 0; pp < PP; ++pp)
+          for (int pp = 0; pp < PP; ++pp)
 #pragma unroll
-              for (int kp = 0; kp < KVP; ++kp)
+            for (int kp = 0; kp < KVP; ++kp)
 #pragma unroll
-                for (int tile = 0; tile < 4; ++tile) {
-                  const uint32_t pacc = (vj > 0 || pp > 0 || kp > 0 || ks > 0) ? 1u : 0u;
-                  const uint64_t ad = pv_a0 + slot_off +
-                                      static_cast<uint64_t>((kp * kKVBytes + (2 * tile) * kChunkBytes + ks * 32 * 64) >> 4);
-                  const uint64_t bd = pp == 0 ? pv_a0 + slot_off + static_cast<uint64_t>((kRope * kChunkBytes + ks * 32 * 64) >> 4)
-                                              : plo0 + static_cast<uint64_t>((ks * 32 * 64) >> 4);
-                  mma_f8f6f4_ss(tmem + tile * kNH, ad, bd, IDESC_PV, pacc);
-                }
-            mma_commit(smem_u32(&s.bar_kv_empty[slot][ks]));
-          }
-          mma_commit(smem_u32(&s.bar_pv_done));
+              for (int tile = 0; tile < 4; ++tile) {
+                const uint32_t pacc = (j > 0 || pp > 0 || kp > 0 || ks > 0) ? 1u : 0u;
+                const uint64_t ad = pv_a0 + slot_off +
+                                    static_cast<uint64_t>((kp * kKVBytes + (2 * tile) * kChunkBytes + ks * 32 * 64) >> 4);
+                const uint64_t bd = pp == 0 ? pv_a0 + slot_off + static_cast<uint64_t>((kRope * kChunkBytes + ks * 32 * 64) >> 4)
+                                            : plo0 + static_cast<uint64_t>((ks * 32 * 64) >> 4);
+                mma_f8f6f4_ss(tmem + tile * kNH, ad, bd, IDESC_PV, pacc);
+              }
+          mma_commit(smem_u32(&s.bar_kv_empty[slot][ks]));
         }
-        ++vj;
-      } else {
-        const uint64_t slot_off = static_cast<uint64_t>(((qj % NST) * KVP * kKVBytes) >> 4);
-        if (leader) {
-          issue_qk<QP, KVP, kSAcc>(tmem + kTmemS, kv_a0 + slot_off, qk_b0, IDESC_QK);
-          mma_commit(smem_u32(&s.bar_s_full));
-        }
-        ++qj;
-        s_free = false;
+        mma_commit(smem_u32(&s.bar_pv_done));
       }
       __syncwarp();
     }
   } else {
     // =================================================================== gather producers
+    setmaxnreg_dec<kLowRegs>();
     const int pt = threadIdx.x - kProdWarp0 * 32;
     const uint32_t first = tok_idx[0];
     const uint64_t keep = make_policy_evict_last();  // the latent pool stays in L2 over the q / out streams
     bool ok = true;
+    // Thread pt < 128 owns row pt of every block: its physical row and scale
+    // are loaded one block ahead.
+    uint32_t nxt_row = 0;
+    float nxt_sr = 1.f;
+    auto load_row = [&](int jb) {
+      const int key = jb * kBK + pt;
+      uint32_t row = key < n ? tok_idx[key] : first;
+      if (row >= static_cast<uint64_t>(p.phys_rows)) {
+        atomicOr(p.err, kErrIndex);
+        row = 0;
+      }
+      nxt_row = row;
+    };
+    auto load_scale = [&]() {
+      if (SC == kRow) {
+        nxt_sr = p.scales[static_cast<int64_t>(nxt_row) * p.nscale];
+      } else if (SC == kBlock) {
+        const float* sp = p.scales + static_cast<int64_t>(nxt_row) * p.nscale;
+        float sr = 0.f;
+        for (int b = 0; b < p.nscale; ++b) sr = fmaxf(sr, sp[b]);
+        nxt_sr = sr > 0.f ? sr : 1.f;
+      }
+    };
+    if (pt < kBK) {
+      load_row(0);
+      load_scale();
+    }
     for (int j = 0; j < nblk; ++j) {
       const int slot = j % NST;
       const uint32_t par = ((j / NST) & 1) ^ 1;
       const bool w = mbar_wait(smem_u32(&s.bar_kv_empty[slot][0]), par, p.err);
       if (!named_bar_and(2, kProdThreads, ok && w)) break;
-      // rows of this block: physical row and scale
-      for (int rr = pt; rr < kBK; rr += kProdThreads) {
-        const int key = j * kBK + rr;
-        uint32_t row = key < n ? tok_idx[key] : first;
-        if (row >= static_cast<uint64_t>(p.phys_rows)) {
-          atomicOr(p.err, kErrIndex);
-          row = 0;
-        }
-        s.idx[rr] = row;
-        float sr = 1.f;
-        if (SC == kRow) {
-          sr = p.scales[static_cast<int64_t>(row) * p.nscale];
-        } else if (SC == kBlock) {
-          const float* sp = p.scales + static_cast<int64_t>(row) * p.nscale;
-          sr = 0.f;
-          for (int b = 0; b < p.nscale; ++b) sr = fmaxf(sr, sp[b]);
-          if (!(sr > 0.f)) sr = 1.f;
-        }
-        s.srow[slot][rr] = sr;
+      if (pt < kBK) {
+        s.idx[pt] = nxt_row;
+        s.srow[slot][pt] = nxt_sr;
       }
       named_bar_sync(2, kProdThreads);
       // Key quarter q (rows 32q..32q+31) is refilled once PV of block j-NST
@@ -655,6 +655,11 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
           }
         }
       }
+      // the next block's row and scale load while this block's rows land
+      if (pt < kBK && j + 1 < nblk) {
+        load_row(j + 1);
+        load_scale();
+      }
       if (KVP == 1) cp_async_wait_all();
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&s.bar_kv_full[slot]));
@@ -674,6 +679,14 @@ static smla_status_t launch_t(const Params& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<QP, KVP, PP, NST, SC>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return fail_cuda(e, "prefill smem attribute");
+  // The register split (setmaxnreg) draws on the launch allocation: refuse a
+  // build whose register count would leave the softmax's increase waiting.
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, prefill_kernel<QP, KVP, PP, NST, SC>);
+  if (e != cudaSuccess) return fail_cuda(e, "prefill attributes");
+  if (fa.numRegs != kLaunchRegs)
+    return fail(SMLA_ERR_UNSUPPORTED, "prefill kernel built with %d registers a thread, the register split needs %d",
+                fa.numRegs, kLaunchRegs);
   dim3 grid(p.T, (p.H + kNH - 1) / kNH);
   prefill_kernel<QP, KVP, PP, NST, SC><<<grid, threads_for(KVP), smem, stream>>>(p);
   e = cudaGetLastError();

@@ -83,6 +83,18 @@ SMLA_DEVICE_INLINE bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) 
   }
 }
 
+// Per-warpgroup register re-allocation (all four warps of a warpgroup
+// execute the same one).  An increase draws on registers released by
+// decreases within the same CTA's launch allocation.
+template <uint32_t N>
+SMLA_DEVICE_INLINE void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+SMLA_DEVICE_INLINE void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // One lane of the (fully active) warp returns true; the same lane every time.
 SMLA_DEVICE_INLINE bool elect_one() {
   uint32_t pred = 0;
