@@ -121,7 +121,7 @@ struct Smem {
   float srow[NST][kBK];  // per-row scale (1 for unit)
   float cs[kNH];         // softmax_scale * log2(e) / 2^e_h
   float mref[kNH];       // reference maximum per head (log2 units)
-  float fac[kNH];        // rescale factor of the current block; row sums at the end
+  float fac[kNH];        // rescale factor of the current block; 1 / row sum at the end
   int mx[2][kNH];        // block maximum per head (order-preserving ints), by block parity
   int rescale[2];
   unsigned long long bar_q, bar_kv_full[NST], bar_kv_empty[NST][kRowQ];
@@ -263,19 +263,23 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
       const bool hvalid = hh < hv;
       float sigma = 1.f;
       if (QP == 2) {
+        // one pass: the thread's 144 bf16 values stay in registers between
+        // the head maximum and the split
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
                                                           (static_cast<int64_t>(t) * p.H + h0 + hh) * kD + qtr * 144);
-        float amax = 0.f;
-        if (hvalid)
-          for (int i = 0; i < 18; ++i) {
-            const uint4 v = ld_stream16(src + i);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint4 v[18];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              amax = fmaxf(amax, fabsf(__uint_as_float(w[k] << 16)));
-              amax = fmaxf(amax, fabsf(__uint_as_float(w[k] & 0xffff0000u)));
-            }
+        for (int i = 0; i < 18; ++i) v[i] = hvalid ? ld_stream16(src + i) : make_uint4(0, 0, 0, 0);
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 18; ++i) {
+          const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            amax = fmaxf(amax, fabsf(__uint_as_float(w[k] << 16)));
+            amax = fmaxf(amax, fabsf(__uint_as_float(w[k] & 0xffff0000u)));
           }
+        }
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         // scale so that the largest |q| * 2^e lies in [128, 256)
@@ -286,19 +290,15 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
           e = 8 - ex;
         }
         sigma = ldexpf(1.f, e);
+#pragma unroll
         for (int i = 0; i < 9; ++i) {
           float x[16];
-          if (hvalid) {
-            const uint4 a = ld_stream16(src + 2 * i), b = ld_stream16(src + 2 * i + 1);
-            const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          const uint32_t w[8] = {v[2 * i].x, v[2 * i].y, v[2 * i].z, v[2 * i].w,
+                                 v[2 * i + 1].x, v[2 * i + 1].y, v[2 * i + 1].z, v[2 * i + 1].w};
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              x[2 * k] = __uint_as_float(w[k] << 16) * sigma;
-              x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u) * sigma;
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 16; ++k) x[k] = 0.f;
+          for (int k = 0; k < 8; ++k) {
+            x[2 * k] = __uint_as_float(w[k] << 16) * sigma;
+            x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u) * sigma;
           }
           uint4 hi, lo;
           split16(x, hi, lo);
@@ -468,25 +468,49 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
       mbar_arrive(smem_u32(&s.bar_p_full));
     }
 
-    // ---- row sums across the 128 key lanes, then O^T / l -> bf16
+    // ---- row sums across the 128 key lanes, then O^T / l -> bf16.  The
+    // output rows of this CTA's heads are contiguous in `out`, so they are
+    // staged in shared memory (slot 0 is dead once the last PV completed)
+    // and written with one bulk copy.
     const bool done =
         named_bar_and(1, kSoftThreads, ok && mbar_wait(smem_u32(&s.bar_pv_done), (nblk - 1) & 1, p.err));
-    float* lsum = s.fac;  // reused as the row-sum accumulator
-    if (threadIdx.x < kNH) lsum[threadIdx.x] = 0.f;
+    // dead slot 0: [64 heads][512] bf16 output stage, then the row-sum partials
+    uint16_t* stage = reinterpret_cast<uint16_t*>(s.kv[0][0]);
+    float(*lpart)[kNH] = reinterpret_cast<float(*)[kNH]>(s.kv[0][0] + kNH * kDV * 2);
+    static_assert(kNH * kDV * 2 + 4 * kNH * 4 <= kKVBytes, "epilogue scratch fits in a slot");
+    {
+      // Transpose-reduce: after log2(32) halving exchanges (31 shuffles),
+      // lane l holds the sum over the warp's 32 key lanes for head hb + l.
+      uint32_t raw[32];
+      tmem_ld32(tmem + lane_base + kTmemL + hb, raw);
+      tmem_wait_ld();
+      float v[32];
+#pragma unroll
+      for (int h = 0; h < 32; ++h) v[h] = __uint_as_float(raw[h]);
+#pragma unroll
+      for (int step = 16; step >= 1; step >>= 1) {
+        const bool upper = (lane & step) != 0;
+#pragma unroll
+        for (int i = 0; i < step; ++i) {
+          const float send = upper ? v[i] : v[i + step];
+          const float keep = upper ? v[i + step] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, step);
+        }
+      }
+      lpart[warp & 3][hb + lane] = v[0];
+    }
     named_bar_sync(1, kSoftThreads);
-    uint32_t lpart[32];
-    tmem_ld32(tmem + lane_base + kTmemL + hb, lpart);
-    tmem_wait_ld();
-#pragma unroll
-    for (int h = 0; h < 32; ++h) {
-      float v = __uint_as_float(lpart[h]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) atomicAdd(&lsum[hb + h], v);
+    float* linv = s.fac;  // reused: 1 / row sum per head
+    if (threadIdx.x < kNH) {
+      const float l = lpart[0][threadIdx.x] + lpart[1][threadIdx.x] + lpart[2][threadIdx.x] + lpart[3][threadIdx.x];
+      linv[threadIdx.x] = l > 0.f ? 1.f / l : 0.f;
     }
     named_bar_sync(1, kSoftThreads);
     if (done) {
       tc_fence_after();
+      float inv[32];
+#pragma unroll
+      for (int h = 0; h < 32; ++h) inv[h] = linv[hb + h];
 #pragma unroll 1
       for (int tile = 0; tile < 4; ++tile) {
         const int vcol = tile * 128 + r;
@@ -494,15 +518,16 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         tmem_ld32(tmem + lane_base + tile * kNH + hb, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 32; ++h) {
-          const int head = hb + h;
-          if (head < hv) {
-            const float l = lsum[head];
-            const float o = l > 0.f ? __uint_as_float(v[h]) / l : 0.f;
-            __stcs(out_t + static_cast<int64_t>(head) * kDV + vcol, __bfloat16_as_ushort(__float2bfloat16_rn(o)));
-          }
-        }
+        for (int h = 0; h < 32; ++h)
+          stage[(hb + h) * kDV + vcol] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[h]) * inv[h]));
       }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1, kSoftThreads);
+    if (done && threadIdx.x == 0) {
+      bulk_store_s2g(out_t, smem_u32(s.kv[0][0]), static_cast<uint32_t>(hv) * kDV * 2);
+      bulk_commit();
+      bulk_wait_all();  // the shared-memory source stays live until the copy is done
     }
   } else if (warp == kMmaWarp) {
     // =================================================================== QK issuer

@@ -323,6 +323,18 @@ SMLA_DEVICE_INLINE bool mbar_wait_cluster(uint32_t bar, uint32_t parity, unsigne
     }
   }
 }
+// Bulk copy (no tensor map) of `bytes` (a multiple of 16, both addresses
+// 16-byte aligned) from this CTA's shared memory to global memory, in a
+// bulk async-group of the issuing thread.  The source must have been made
+// visible to the async proxy (fence.proxy.async after the writes).
+SMLA_DEVICE_INLINE void bulk_store_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+SMLA_DEVICE_INLINE void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until every bulk group of this thread has completed (writes done).
+SMLA_DEVICE_INLINE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 SMLA_DEVICE_INLINE void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
