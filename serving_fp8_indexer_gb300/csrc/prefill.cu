@@ -84,7 +84,7 @@ constexpr int kProdWarp0 = 10;
 __host__ __device__ constexpr int prod_warps(int) { return 14; }
 __host__ __device__ constexpr int threads_for(int kvp) { return kSoftThreads + 64 + 32 * prod_warps(kvp); }
 constexpr int kLaunchRegs = 80;
-constexpr int kSoftRegs = 152;
+constexpr int kSoftRegs = 160;
 constexpr int kLowRegs = 40;
 static_assert(kSoftThreads * kSoftRegs + (threads_for(1) - kSoftThreads) * kLowRegs <= threads_for(1) * kLaunchRegs,
               "register split exceeds the launch allocation");
@@ -120,10 +120,10 @@ struct Smem {
   uint32_t idx[kBK];
   float srow[NST][kBK];  // per-row scale (1 for unit)
   float cs[kNH];         // softmax_scale * log2(e) / 2^e_h
-  float mref[kNH];       // reference maximum per head (log2 units)
+  float negm[kNH];       // minus the reference maximum per head (log2 units)
+  float delta[kNH];      // reference raise of the current block
   float fac[kNH];        // rescale factor of the current block; 1 / row sum at the end
-  int mx[2][kNH];        // block maximum per head (order-preserving ints), by block parity
-  int rescale[2];
+  int mx[kNH];           // block maximum per head (order-preserving ints)
   unsigned long long bar_q, bar_kv_full[NST], bar_kv_empty[NST][kRowQ];
   unsigned long long bar_s_full, bar_s_free, bar_p_full, bar_pv_done;
   uint32_t tmem_base;
@@ -196,9 +196,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
   // its accumulator but not for other MMAs (measured: two alternating
   // accumulators already run a block's QK as fast as three).
   constexpr int kSAcc = 2;
-  // per-lane partial row sums live in TMEM after the S accumulators
-  constexpr uint32_t kTmemL = kTmemS + kNH * kSAcc;
-  static_assert(kTmemL + kNH <= kTmemCols, "TMEM budget");
+  static_assert(kTmemS + kNH * kSAcc <= kTmemCols, "TMEM budget");
   constexpr int kThreads = threads_for(KVP);
   constexpr int kProdThreads = 32 * prod_warps(KVP);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -237,10 +235,9 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     mbar_init(smem_u32(&s.bar_s_free), kSoftThreads);
     mbar_init(smem_u32(&s.bar_p_full), kSoftThreads);
     mbar_init(smem_u32(&s.bar_pv_done), 1);
-    s.rescale[0] = s.rescale[1] = 0;
     fence_mbar_init();
   }
-  if (threadIdx.x < 2 * kNH) (&s.mx[0][0])[threadIdx.x] = kOrdMin;
+  if (threadIdx.x < kNH) s.mx[threadIdx.x] = kOrdMin;
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&s.tmem_base), kTmemCols);
     tmem_relinquish();
@@ -320,20 +317,18 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
       }
       if (qtr == 0) {
         s.cs[hh] = p.softmax_scale * kLog2e / sigma;
-        s.mref[hh] = -INFINITY;
+        s.negm[hh] = 0.f;  // block 0 sets the reference
       }
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&s.bar_q));
     }
     named_bar_sync(1, kSoftThreads);
 
-    {
-      uint32_t zero[32];
+    // lv[h]: this key lane's share of head hb+h's softmax denominator, summed
+    // over the blocks (P / s_row, in the current reference's units)
+    float lv[32];
 #pragma unroll
-      for (int h = 0; h < 32; ++h) zero[h] = 0u;
-      tmem_st32(tmem + lane_base + kTmemL + hb, zero);
-      tmem_wait_st();
-    }
+    for (int h = 0; h < 32; ++h) lv[h] = 0.f;
     bool ok = true;
 
     for (int j = 0; ok && j < nblk; ++j) {
@@ -344,84 +339,100 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
                mbar_wait(smem_u32(&s.bar_kv_full[slot]), (j / NST) & 1, p.err);
       if (!named_bar_and(1, kSoftThreads, w)) { ok = false; break; }
       tc_fence_after();
-      float z[32];
+      float y[32];
       {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + kTmemS + hb, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 32; ++h) z[h] = __uint_as_float(v[h]);
+        for (int h = 0; h < 32; ++h) y[h] = __uint_as_float(v[h]);
 #pragma unroll
         for (int a = 1; a < kSAcc; ++a) {
           tmem_ld32(tmem + lane_base + kTmemS + a * kNH + hb, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 32; ++h) z[h] += __uint_as_float(v[h]);
+          for (int h = 0; h < 32; ++h) y[h] += __uint_as_float(v[h]);
         }
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&s.bar_s_free));  // S may now be overwritten by QK of block j+1
-      const bool valid = j * kBK + r < n;
       const float sr = SC == kUnit ? 1.f : s.srow[slot][r];
       const float lg = SC == kUnit ? 0.f : __log2f(sr);
-      // z = logit in log2 units; z + log2(s_row) is the PV operand's exponent.
-      // Fast path: no element exceeds its head's reference by more than tau.
-      bool ex = false;
+      // y = logit (log2 units) minus the head's reference maximum m_h,
+      //   y = S * s_row * c_h - m_h,
+      // and the PV operand is exp2(y + log2 s_row).  Block 0 has m = 0: it
+      // computes the logits themselves and sets the references to its maxima.
+      float ymax = -INFINITY;
+      {
+        const float4* c4p = reinterpret_cast<const float4*>(s.cs + hb);
+        const float4* m4p = reinterpret_cast<const float4*>(s.negm + hb);
 #pragma unroll
-      for (int h = 0; h < 32; ++h) {
-        z[h] = valid ? z[h] * (sr * s.cs[hb + h]) : -INFINITY;
-        ex |= z[h] + lg > s.mref[hb + h] + kTau;
+        for (int q = 0; q < 8; ++q) {
+          const float4 c = c4p[q], m = m4p[q];
+          const float cc[4] = {c.x, c.y, c.z, c.w}, mm[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int h = 4 * q + k;
+            y[h] = fmaf(y[h], SC == kUnit ? cc[k] : sr * cc[k], mm[k]);
+            ymax = fmaxf(ymax, y[h]);
+          }
+        }
       }
-      if (named_bar_or(1, kSoftThreads, ex)) {
-        // Slow path (always taken by the first block): block maximum per head
-        // across the 128 key lanes, raise the references that it exceeds.
+      if ((j + 1) * kBK > n && j * kBK + r >= n) {  // lanes past the selection (last block only)
+#pragma unroll
+        for (int h = 0; h < 32; ++h) y[h] = -INFINITY;
+        ymax = -INFINITY;
+      }
+      // Fast path: no element exceeds its head's reference by more than tau.
+      if (named_bar_or(1, kSoftThreads, j == 0 || ymax + lg > kTau)) {
+        // Slow path (always taken by block 0): t_h = block maximum of y + lg
+        // per head across the 128 key lanes.  Block 0 sets m_h = t_h; a
+        // later block raises m_h by t_h where t_h > tau and scales O^T and
+        // the row sums of that head by exp2(-t_h).
         int mine = kOrdMin;
 #pragma unroll
         for (int h = 0; h < 32; ++h) {
-          const int m = __reduce_max_sync(0xffffffffu, ord_int(z[h] + lg));
+          const int m = __reduce_max_sync(0xffffffffu, ord_int(y[h] + lg));
           if (lane == h) mine = m;
         }
-        atomicMax(&s.mx[0][hb + lane], mine);
+        atomicMax(&s.mx[hb + lane], mine);
         named_bar_sync(1, kSoftThreads);
         if ((warp & 3) == 0) {
           const int hh = hb + lane;
-          const float mb = ord_float(s.mx[0][hh]);
-          s.mx[0][hh] = kOrdMin;
-          const float old = s.mref[hh];
-          float f = 1.f;
-          if (mb > old + kTau) {
-            s.mref[hh] = mb;
-            f = exp2f(old - mb);  // 0 when old is -inf
+          const float t = ord_float(s.mx[hh]);
+          s.mx[hh] = kOrdMin;
+          float d = 0.f, f = 1.f;
+          if (j == 0 || t > kTau) {
+            d = t;
+            if (j > 0) f = exp2f(-t);
+            s.negm[hh] -= t;
           }
+          s.delta[hh] = d;
           s.fac[hh] = f;
         }
         named_bar_sync(1, kSoftThreads);
+#pragma unroll
+        for (int h = 0; h < 32; ++h) y[h] -= s.delta[hb + h];
         if (j > 0) {
+#pragma unroll
+          for (int h = 0; h < 32; ++h) lv[h] *= s.fac[hb + h];
           // O^T holds blocks < j: wait for the last PV, then scale each head's column.
           w = mbar_wait(smem_u32(&s.bar_pv_done), (j - 1) & 1, p.err);
           if (!named_bar_and(1, kSoftThreads, w)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
-          for (int tile = 0; tile < 4; ++tile) {
-            uint32_t v[32];
-            const uint32_t a = tmem + lane_base + tile * kNH + hb;
-            tmem_ld32(a, v);
+          for (int part = 0; part < 8; ++part) {  // 4 tiles x 2 halves of this warp's 32 heads
+            uint32_t v[16];
+            const int c0 = (part & 1) * 16;
+            const uint32_t a = tmem + lane_base + (part >> 1) * kNH + hb + c0;
+            tmem_ld16(a, v);
             tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < 32; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * s.fac[hb + h]);
-            tmem_st32(a, v);
+            for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * s.fac[hb + c0 + h]);
+            tmem_st16(a, v);
           }
           tmem_wait_st();
           tc_fence_before();
-          {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + kTmemL + hb, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int h = 0; h < 32; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * s.fac[hb + h]);
-            tmem_st32(tmem + lane_base + kTmemL + hb, v);
-            tmem_wait_st();
-          }
         }
       }
       // ---- P row r (this thread's 32 heads) and the row sums
@@ -431,18 +442,12 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         float x[16];
-        uint32_t lv[16];
-        const uint32_t la = tmem + lane_base + kTmemL + hb + c * 16;
-        tmem_ld16(la, lv);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           const int h = c * 16 + k;
-          x[k] = ex2_approx(z[h] + lg - s.mref[hb + h]);   // 0 for invalid rows
+          x[k] = ex2_approx(SC == kUnit ? y[h] : y[h] + lg);  // 0 past the selection
+          lv[h] = SC == kUnit ? lv[h] + x[k] : fmaf(x[k], isr, lv[h]);
         }
-        tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 16; ++k) lv[k] = __float_as_uint(fmaf(x[k], isr, __uint_as_float(lv[k])));
-        tmem_st16(la, lv);
         const int c4 = half * 2 + c;
         if (PP == 2) {
           uint4 hi;
@@ -463,7 +468,6 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
 #pragma unroll
         for (int c = 0; c < 2; ++c) *reinterpret_cast<uint4*>(s.plo + r * 64 + sw64(r, half * 2 + c)) = lo_keep[c];
       }
-      tmem_wait_st();
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&s.bar_p_full));
     }
@@ -481,23 +485,17 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     {
       // Transpose-reduce: after log2(32) halving exchanges (31 shuffles),
       // lane l holds the sum over the warp's 32 key lanes for head hb + l.
-      uint32_t raw[32];
-      tmem_ld32(tmem + lane_base + kTmemL + hb, raw);
-      tmem_wait_ld();
-      float v[32];
-#pragma unroll
-      for (int h = 0; h < 32; ++h) v[h] = __uint_as_float(raw[h]);
 #pragma unroll
       for (int step = 16; step >= 1; step >>= 1) {
         const bool upper = (lane & step) != 0;
 #pragma unroll
         for (int i = 0; i < step; ++i) {
-          const float send = upper ? v[i] : v[i + step];
-          const float keep = upper ? v[i + step] : v[i];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, step);
+          const float send = upper ? lv[i] : lv[i + step];
+          const float keep = upper ? lv[i + step] : lv[i];
+          lv[i] = keep + __shfl_xor_sync(0xffffffffu, send, step);
         }
       }
-      lpart[warp & 3][hb + lane] = v[0];
+      lpart[warp & 3][hb + lane] = lv[0];
     }
     named_bar_sync(1, kSoftThreads);
     float* linv = s.fac;  // reused: 1 / row sum per head
@@ -527,7 +525,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     if (done && threadIdx.x == 0) {
       bulk_store_s2g(out_t, smem_u32(s.kv[0][0]), static_cast<uint32_t>(hv) * kDV * 2);
       bulk_commit();
-      bulk_wait_all();  // the shared-memory source stays live until the copy is done
+      bulk_wait_read_all();  // the shared-memory source stays live until the copy has read it
     }
   } else if (warp == kMmaWarp) {
     // =================================================================== QK issuer

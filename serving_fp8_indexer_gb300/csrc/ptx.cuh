@@ -332,8 +332,9 @@ SMLA_DEVICE_INLINE void bulk_store_s2g(void* dst, uint32_t src, uint32_t bytes) 
                : "memory");
 }
 SMLA_DEVICE_INLINE void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Waits until every bulk group of this thread has completed (writes done).
-SMLA_DEVICE_INLINE void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Waits until every bulk group of this thread has read its shared-memory
+// source (the global writes complete asynchronously, before the kernel ends).
+SMLA_DEVICE_INLINE void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 SMLA_DEVICE_INLINE void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
