@@ -17,9 +17,11 @@ data path); rank 0 prints.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -42,6 +44,23 @@ def load_peaks():
         except Exception:
             pass
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def profiled_traffic(kernel_src, profile_md, captured_tokens, tokens):
+    """DRAM bytes per launch from a committed ncu summary (read + write of a
+    smaller launch of the same kernel variant), scaled by the tokens a launch
+    processes.  None once the kernel source differs from the one captured."""
+    try:
+        src = open(os.path.join(ROOT, kernel_src), "rb").read()
+        md = open(os.path.join(ROOT, profile_md)).read()
+    except OSError:
+        return None
+    if hashlib.sha1(src).hexdigest() not in md:
+        return None
+    m = re.search(r"`dram__bytes_read.sum` / `dram__bytes_write.sum` \| ([0-9.]+) MB / ([0-9.]+) MB", md)
+    if not m:
+        return None
+    return (float(m.group(1)) + float(m.group(2))) * 1e6 * tokens / captured_tokens
 
 
 def peak_value(peaks, key):
@@ -422,7 +441,12 @@ def run_ours(args, rank, world):
                                 "unit": "keys·tok/s"}
     if "sparse_mla" in stage:
         tf = stages["sparse_mla"]["TFLOP/s"]
+        # measured DRAM traffic, only for the variant the committed capture covers
+        # (128 heads, bf16 q, tensorwise scale: the end-to-end chunk's shapes)
         traffic = None
+        if args.case in ("chunk", "chunk_small"):
+            traffic = profiled_traffic("serving_fp8_indexer_gb300/csrc/prefill.cu",
+                                       "profiles/prefill_kernel_chunk_small.md", 1024, int(w.seqs.T))
         line["roofline"] = {"bound": "tensor", "kernel": "prefill_kernel (sparse MLA)", "achieved": tf,
                             "peak": bf16_peak, "unit": "TFLOP/s", "frac": tf / bf16_peak, "traffic": traffic,
                             "peak_source": f"{src} bf16 dense (sustained)"}
