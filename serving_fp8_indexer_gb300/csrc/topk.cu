@@ -9,12 +9,15 @@
 //     order-preserving 32-bit keys;
 //   * the row's min/max (taken while loading) give the highest bit in which
 //     the keys differ; one 11-bit histogram pass over the row from there
-//     finds the bin holding the k-th largest, whose keys are then collected
-//     into a short candidate list where the remaining digits are resolved
-//     (the row is re-scanned only if that list overflows);
-//   * one stable compaction pass in logical-key order (warp ballots over
-//     warp-contiguous key ranges) emits every key above that value plus the
-//     lowest-keyed ties, mapped to physical rows through the page table.
+//     finds the bin holding the k-th largest;
+//   * one pass over warp-contiguous key ranges counts each range's keys
+//     above that bin and lists the bin's keys (the candidates);
+//   * a short candidate list is ranked directly (score descending, key
+//     ascending: the lowest-keyed ties win), marking the taken ones in a
+//     bitmap; a long one falls back to more 11-bit digit passes;
+//   * one stable compaction pass in logical-key order (warp ballots over the
+//     same ranges) emits every key above the bin plus the taken candidates,
+//     mapped to physical rows through the page table.
 // Tokens with pos + 1 <= k take every valid key without selecting.
 #include <algorithm>
 
@@ -28,6 +31,7 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kBinsPerThread = kBins / kThreads;
+constexpr int kRankCap = 128;  // candidates ranked pairwise; longer lists take more digit passes
 
 struct Params {
   const float* scores;
@@ -36,6 +40,7 @@ struct Params {
   const int32_t* kv_len;
   const int32_t* page_table;
   int B, max_pages, page_size, T;
+  int page_shift;  // log2(page_size)
   int k;
   uint32_t* indices;
   uint32_t* lens;
@@ -82,13 +87,29 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* t
 }
 
 __device__ __forceinline__ uint32_t phys_row(const Params& p, int b, int key) {
-  const int page = key / p.page_size;
+  const int page = key >> p.page_shift;
   const int pid = page < p.max_pages ? p.page_table[static_cast<int64_t>(b) * p.max_pages + page] : -1;
   if (pid < 0) {
     atomicOr(p.err, kErrPage);
     return 0xFFFFFFFFu;
   }
-  return static_cast<uint32_t>(pid) * static_cast<uint32_t>(p.page_size) + static_cast<uint32_t>(key % p.page_size);
+  return (static_cast<uint32_t>(pid) << p.page_shift) | static_cast<uint32_t>(key & (p.page_size - 1));
+}
+
+// Writes the physical row of logical key i to out[o] (page ids from the
+// shared-memory copy `ptab` when it holds the sequence's pages).
+__device__ __forceinline__ void emit(const Params& p, int b, const int* ptab, uint32_t* out, int o, int i) {
+  if (o >= p.k) {
+    atomicOr(p.err, kErrShape);
+    return;
+  }
+  if (ptab) {
+    const int pid = ptab[i >> p.page_shift];
+    out[o] = pid >= 0 ? (static_cast<uint32_t>(pid) << p.page_shift) | static_cast<uint32_t>(i & (p.page_size - 1))
+                      : phys_row(p, b, i);
+  } else {
+    out[o] = phys_row(p, b, i);
+  }
 }
 
 // Finds the digit bin holding the krem-th largest candidate (bins counted
@@ -119,7 +140,7 @@ __device__ __forceinline__ int select_bin(const uint32_t* hist, int& krem, int* 
   return bin;
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 3) topk_kernel(const Params p) {
   extern __shared__ uint32_t smem_dyn[];
   uint32_t* cache = smem_dyn;                 // the row, as ordered keys
   uint32_t* cand = smem_dyn + p.cache_cap;    // candidate list
@@ -193,11 +214,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const Params p) {
   }
   auto key_at = [&](int i) -> uint32_t { return cached ? cache[i] : ordered(row[i]); };
 
-  // ---- exact k-th largest ordered key.  Bits above the highest bit in
-  // which the row's keys differ are common to every key, so the first
-  // 11-bit digit starts there.  One histogram pass over the row finds the
-  // digit bin holding the k-th largest; the keys of that bin are collected
-  // into a short candidate list on which the remaining digits are resolved.
+  // ---- the bin of the k-th largest ordered key.  Bits above the highest
+  // bit in which the row's keys differ are common to every key, so the first
+  // 11-bit digit starts there.
   kmin = __reduce_min_sync(0xffffffffu, kmin);
   kmax = __reduce_max_sync(0xffffffffu, kmax);
   if ((tid & 31) == 0) {
@@ -214,6 +233,11 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const Params p) {
     kmin = min(kmin, s_wmin[w]);
     kmax = max(kmax, s_wmax[w]);
   }
+  const int lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
+  // warp w owns the keys [w*span, (w+1)*span); lane l reads key base + 32m + l
+  const int span = ((n + kWarps - 1) / kWarps + 31) & ~31;
+  const int w0 = min(n, warp * span), w1 = min(n, w0 + span);
   const uint32_t diff = kmin ^ kmax;
   int krem = k;
   uint32_t thr = kmax;  // all keys equal: every key is a tie of kmax
@@ -230,53 +254,100 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const Params p) {
     hi_val |= static_cast<uint32_t>(bin) << sh;
     hi_mask |= dmask << sh;
     top = sh - 1;
-    if (top >= 0) {
-      // candidates: the keys of the chosen bin (the same digit prefix)
-      const int ncand_cap = p.cand_cap;
-      for (int i = tid; i < n; i += kThreads) {
-        const uint32_t u = key_at(i);
-        if ((u & hi_mask) == hi_val) {
-          const int slot = atomicAdd(&s_ncand, 1);
-          if (slot < ncand_cap) cand[slot] = u;
+    // krem keys are still to be taken from the bin (hi_val, hi_mask); every key
+    // above the bin's largest value is taken
+    const uint32_t bin_max = hi_val | ~hi_mask;
+    // ---- candidates: count each range's keys above the bin, list the bin's keys
+    int nabove = 0;
+    const int ncand_cap = p.cand_cap;
+    for (int base = w0; base < w1; base += 32) {
+      const int i = base + lane;
+      const uint32_t u = i < w1 ? key_at(i) : 0u;
+      nabove += __popc(__ballot_sync(0xffffffffu, i < w1 && u > bin_max));
+      const bool inb = i < w1 && (u & hi_mask) == hi_val;
+      const uint32_t bm = __ballot_sync(0xffffffffu, inb);
+      if (bm) {
+        int c0 = 0;
+        if (lane == 0) c0 = atomicAdd(&s_ncand, __popc(bm));
+        c0 = __shfl_sync(0xffffffffu, c0, 0);
+        const int slot = c0 + __popc(bm & lt);
+        if (inb && slot < ncand_cap) cand[slot] = static_cast<uint32_t>(i);
+      }
+    }
+    __syncthreads();  // s_wmin / s_wmax / hist are reused below
+    const int nc = s_ncand;
+    if (nc <= kRankCap && n <= kBins * 32) {
+      // ---- short list: rank each candidate by (score desc, key asc); the
+      // first krem are taken, marked in a bitmap (hist reused) and counted
+      // per warp range.
+      uint32_t* taken = hist;
+      int* above_w = reinterpret_cast<int*>(s_wmin);
+      int* cand_w = reinterpret_cast<int*>(s_wmax);
+      for (int i = tid; i < (n + 31) / 32; i += kThreads) taken[i] = 0u;
+      if (lane == 0) above_w[warp] = nabove;
+      if (tid < kWarps) cand_w[tid] = 0;
+      __syncthreads();
+      for (int c = tid; c < nc; c += kThreads) {
+        const int ic = static_cast<int>(cand[c]);
+        const uint32_t uc = key_at(ic);
+        int rank = 0;
+        for (int d = 0; d < nc; ++d) {
+          const int id = static_cast<int>(cand[d]);
+          const uint32_t ud = key_at(id);
+          rank += (ud > uc || (ud == uc && id < ic)) ? 1 : 0;
+        }
+        if (rank < krem) {
+          atomicOr(&taken[ic >> 5], 1u << (ic & 31));
+          atomicAdd(&cand_w[ic / span], 1);
         }
       }
       __syncthreads();
-      const int nc = s_ncand;
-      const bool in_list = nc <= ncand_cap;
-      while (top >= 0) {
-        sh = max(0, top - 10);
-        dmask = (1u << (top - sh + 1)) - 1u;
-        for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
-        __syncthreads();
-        if (in_list) {
-          for (int i = tid; i < nc; i += kThreads) {
-            const uint32_t u = cand[i];
-            if ((u & hi_mask) == hi_val) atomicAdd(&hist[(u >> sh) & dmask], 1u);
-          }
-        } else {
-          for (int i = tid; i < n; i += kThreads) {
-            const uint32_t u = key_at(i);
-            if ((u & hi_mask) == hi_val) atomicAdd(&hist[(u >> sh) & dmask], 1u);
-          }
-        }
-        __syncthreads();
-        bin = select_bin(hist, krem, warp_tot, &sh_bin, &sh_above);
-        hi_val |= static_cast<uint32_t>(bin) << sh;
-        hi_mask |= dmask << sh;
-        top = sh - 1;
+      // ---- one stable compaction pass in logical-key order
+      int pos = 0;
+      for (int w = 0; w < warp; ++w) pos += above_w[w] + cand_w[w];
+      for (int base = w0; base < w1; base += 32) {
+        const int i = base + lane;
+        const uint32_t u = i < w1 ? key_at(i) : 0u;
+        const bool sel = i < w1 && (u > bin_max || ((u & hi_mask) == hi_val && ((taken[i >> 5] >> (i & 31)) & 1u)));
+        const uint32_t bsel = __ballot_sync(0xffffffffu, sel);
+        if (sel) emit(p, b, pt_cached ? ptab : nullptr, out, pos + __popc(bsel & lt), i);
+        pos += __popc(bsel);
       }
+      if (tid == 0) p.lens[t] = static_cast<uint32_t>(k);
+      return;
+    }
+    // ---- long list: resolve the remaining digits on the candidates (or on
+    // the whole row when the list overflowed), then the two-pass compaction
+    const bool in_list = nc <= ncand_cap;
+    while (top >= 0) {
+      sh = max(0, top - 10);
+      dmask = (1u << (top - sh + 1)) - 1u;
+      for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+      __syncthreads();
+      if (in_list) {
+        for (int i = tid; i < nc; i += kThreads) {
+          const uint32_t u = key_at(static_cast<int>(cand[i]));
+          if ((u & hi_mask) == hi_val) atomicAdd(&hist[(u >> sh) & dmask], 1u);
+        }
+      } else {
+        for (int i = tid; i < n; i += kThreads) {
+          const uint32_t u = key_at(i);
+          if ((u & hi_mask) == hi_val) atomicAdd(&hist[(u >> sh) & dmask], 1u);
+        }
+      }
+      __syncthreads();
+      bin = select_bin(hist, krem, warp_tot, &sh_bin, &sh_above);
+      hi_val |= static_cast<uint32_t>(bin) << sh;
+      hi_mask |= dmask << sh;
+      top = sh - 1;
     }
     thr = hi_val;
   }
   // thr = exact k-th largest key; krem of its ties are taken (lowest keys first)
 
-  // ---- stable compaction in logical-key order.  Warp w owns the keys
-  // [w*span, (w+1)*span); lane l reads key base + 32m + l (conflict-free),
-  // and warp ballots keep the output in key order.
+  // ---- stable compaction in logical-key order, two passes: per-range counts
+  // of keys above thr and of ties, then the ballot-ordered writes.
   __syncthreads();  // s_wmin / s_wmax are reused below
-  const int lane = tid & 31, warp = tid >> 5;
-  const int span = ((n + kWarps - 1) / kWarps + 31) & ~31;
-  const int w0 = min(n, warp * span), w1 = min(n, w0 + span);
   int ngt = 0, neq = 0;
   for (int base = w0; base < w1; base += 32) {
     const int i = base + lane;
@@ -295,7 +366,6 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const Params p) {
     sel_base += g + max(0, min(e, krem - tie_base));
     tie_base += e;
   }
-  const uint32_t lt = (1u << lane) - 1u;
   int pos = sel_base, tie = tie_base;
   for (int base = w0; base < w1; base += 32) {
     const int i = base + lane;
@@ -305,20 +375,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const Params p) {
     const int my_tie = tie + __popc(beq & lt);
     const bool sel = gt || (eq && my_tie < krem);
     const uint32_t bsel = __ballot_sync(0xffffffffu, sel);
-    if (sel) {
-      const int o = pos + __popc(bsel & lt);
-      if (o < k) {
-        if (pt_cached) {
-          const int pid = ptab[i / p.page_size];
-          out[o] = pid >= 0 ? static_cast<uint32_t>(pid) * static_cast<uint32_t>(p.page_size) +
-                                  static_cast<uint32_t>(i % p.page_size)
-                            : phys_row(p, b, i);
-        } else {
-          out[o] = phys_row(p, b, i);
-        }
-      }
-      else atomicOr(p.err, kErrShape);
-    }
+    if (sel) emit(p, b, pt_cached ? ptab : nullptr, out, pos + __popc(bsel & lt), i);
     pos += __popc(bsel);
     tie += __popc(beq);
   }
@@ -341,8 +398,8 @@ smla_status_t launch_topk(const float* scores, int64_t score_stride, const smla_
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return fail_cuda(e, "topk smem attribute");
   Params p{scores, score_stride, seqs.cu_q, seqs.kv_len, seqs.page_table, seqs.B, seqs.max_pages,
-           seqs.page_size, seqs.T, k, indices, topk_lengths, static_cast<int>(cap), static_cast<int>(cand_cap),
-           static_cast<int>(pt_cap), err};
+           seqs.page_size, seqs.T, __builtin_ctz(static_cast<unsigned>(seqs.page_size)), k, indices, topk_lengths,
+           static_cast<int>(cap), static_cast<int>(cand_cap), static_cast<int>(pt_cap), err};
   topk_kernel<<<seqs.T, kThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, "topk launch");
