@@ -16,10 +16,15 @@
 //     is read in place.  Key tiles wholly past the last token's position
 //     are not computed, only filled with -inf.
 //   * Two TMEM accumulators (2 x 256 columns) let the MMA of tile i+1 run
-//     while 8 epilogue warps drain tile i: relu, x q_scale, sum over the
-//     token's heads, x k_scale, causal -inf, coalesced f32 stores.
+//     while the epilogue warps drain tile i (each: one TMEM lane quarter x
+//     one column slice): relu, x q_scale, sum over the token's heads,
+//     x k_scale, causal -inf, coalesced f32 stores.  The
+//     item's page ids are staged in shared memory and each lane's k_scale
+//     is loaded two tiles ahead, so no L2 round trip sits in a tile's
+//     epilogue (measured: with the lookup inline, the epilogue waited on it
+//     and a tile took ~4x its MMA time).
 //   * Warp roles: warp 0 TMA producer, warp 1 MMA issuer (and TMEM owner),
-//     warps 2..9 epilogue.
+//     warps 2.. epilogue.
 #include <algorithm>
 
 #include "ptx.cuh"
@@ -32,9 +37,15 @@ constexpr int kDepth = 128;
 constexpr int kBM = 128;      // keys per tile (MMA M)
 constexpr int kBN = 256;      // (token, head) columns per tile (MMA N)
 constexpr int kStages = 4;
-constexpr int kThreads = 320;
-constexpr int kEpiThreads = 256;
+// Epilogue warps (a multiple of 4: one per TMEM lane quarter and column
+// slice).  Measured on the end-to-end chunk: 8 warps 1.67 ms, 16 warps
+// 1.94 ms.
+constexpr int kEpiThreads = 32 * 8;
+constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kSlices = kEpiThreads / 128;   // column slices; 4 TMEM lane quarters each
+constexpr int kSliceCols = kBN / kSlices;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxItemPages = 1024;  // the host sizes key chunks to stay within this
 
 struct Params {
   const float* q_scale;
@@ -44,6 +55,7 @@ struct Params {
   const int32_t* kv_len;
   const int32_t* page_table;
   int B, max_pages, page_size, T;
+  int page_shift;  // log2(page_size)
   float* scores;
   int64_t score_stride;
   int chunk_tiles;  // key tiles per work item
@@ -55,6 +67,7 @@ struct __align__(1024) Smem {
   uint8_t q[kBN * kDepth];            // SW128 K-major: 256 rows x 128 B
   uint8_t k[kStages][kBM * kDepth];   // SW128 K-major: 128 rows x 128 B each
   float qs[kBN];
+  int pages[kMaxItemPages];           // page ids of the item's key chunk
   unsigned long long bar_q, bar_kfull[kStages], bar_kempty[kStages], bar_afull[2], bar_aempty[2], bar_drain;
   uint32_t tmem_base;
   int item_b, item_tt, item_kc;
@@ -65,7 +78,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const Params p) {
   constexpr int TOK = kBN / HIDX;      // tokens per tile
-  constexpr int HALF_TOK = TOK / 2;    // tokens per epilogue column half
+  constexpr int SLICE_TOK = kSliceCols / HIDX;  // tokens per epilogue column slice
   constexpr uint32_t IDESC = idesc_e4m3_f32(kBM, kBN, 0, 0);
 
   extern __shared__ uint8_t smem_raw[];
@@ -153,10 +166,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&s.tmem_base), kTmemCols);
     tmem_relinquish();
   }
+  // pages of the keys [key_lo, key_lo + CW) (-1 past the sequence's table)
+  const int page_lo = key_lo >> p.page_shift;
+  const int npg = min(kMaxItemPages, ((key_lo + CW - 1) >> p.page_shift) - page_lo + 1);
   if (warp >= 2) {
-    const int c = threadIdx.x - 64;  // 0..255 = column (token-in-tile, head)
-    const int tok = c / HIDX, h = c % HIDX;
-    s.qs[c] = (tok < ntok) ? p.q_scale[static_cast<int64_t>(t0 + tok) * HIDX + h] : 0.f;
+    const int c = threadIdx.x - 64;  // column (token-in-tile, head)
+    if (c < kBN) {
+      const int tok = c / HIDX, h = c % HIDX;
+      s.qs[c] = (tok < ntok) ? p.q_scale[static_cast<int64_t>(t0 + tok) * HIDX + h] : 0.f;
+    }
+    for (int i = c; i < npg; i += kEpiThreads) {
+      const int pg = page_lo + i;
+      s.pages[i] = pg < p.max_pages ? p.page_table[static_cast<int64_t>(b) * p.max_pages + pg] : -1;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -225,47 +247,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int ew = warp - 2;           // 0..7
+    const int ew = warp - 2;
     const int quarter = warp & 3;      // TMEM lanes this warp may access
-    const int half = ew >> 2;          // column half: tokens [half*HALF_TOK, +HALF_TOK)
+    const int slice = ew >> 2;         // columns [slice*kSliceCols, +kSliceCols)
     const int row = quarter * 32 + lane;
-    const float* qs = s.qs + half * (kBN / 2);
+    const float* qs = s.qs + slice * kSliceCols;
+    // k_scale of this lane's key (physical row) in tile i, from the staged page ids
+    auto load_ks = [&](int i) -> float {
+      const int key = (kt_begin + i) * kBM + row;
+      if (i >= n_tiles || key >= kvl) return 0.f;
+      const int pi = (key >> p.page_shift) - page_lo;
+      const int pid = pi < npg ? s.pages[pi] : -1;
+      const int64_t prow = (static_cast<int64_t>(pid) << p.page_shift) + (key & (p.page_size - 1));
+      return (pid >= 0 && prow < p.phys_rows) ? __ldg(p.k_scale + prow) : 0.f;
+    };
+    float ks_next = load_ks(0), ks_next2 = load_ks(1);
     for (int i = 0; i < n_tiles; ++i) {
       const int a = i & 1;
       const int kt = kt_begin + i;
       const int key = kt * kBM + row;
-      // k_scale of this lane's key (physical row) while the MMA runs.
-      float ks = 0.f;
-      if (key < kvl) {
-        const int page = key / p.page_size;
-        const int pid = page < p.max_pages ? p.page_table[static_cast<int64_t>(b) * p.max_pages + page] : -1;
-        const int64_t prow = static_cast<int64_t>(pid) * p.page_size + key % p.page_size;
-        if (pid >= 0 && prow < p.phys_rows) ks = p.k_scale[prow];
-      }
+      const float ks = ks_next;
+      ks_next = ks_next2;
+      ks_next2 = load_ks(i + 2);
       // warp-uniform: the tcgen05.ld below is warp-collective
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_afull[a]), (i >> 1) & 1, p.err))) break;
       tc_fence_after();
-      float acc[HALF_TOK];
+      float acc[SLICE_TOK];
 #pragma unroll
-      for (int j = 0; j < HALF_TOK; ++j) acc[j] = 0.f;
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * kBN + half * (kBN / 2);
+      for (int j = 0; j < SLICE_TOK; ++j) acc[j] = 0.f;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * kBN + slice * kSliceCols;
 #pragma unroll
-      for (int cb = 0; cb < kBN / 2; cb += 32) {
-        uint32_t v[32];
-        tmem_ld32(taddr + cb, v);
+      for (int cb = 0; cb < kSliceCols; cb += 64) {
+        // two loads in flight per wait
+        uint32_t v[64];
+        tmem_ld32(taddr + cb, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld32(taddr + cb + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float x = fmaxf(__uint_as_float(v[j]), 0.f);
-          acc[(cb + j) / HIDX] = fmaf(x, qs[cb + j], acc[(cb + j) / HIDX]);
+        for (int j = 0; j < 64; j += 4) {
+          const float4 q4 = *reinterpret_cast<const float4*>(qs + cb + j);
+          const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int tj = (cb + j + u) / HIDX;
+            acc[tj] = fmaf(fmaxf(__uint_as_float(v[j + u]), 0.f), qq[u], acc[tj]);
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&s.bar_aempty[a]));
       if (key >= key_lo && key < cover_hi) {
 #pragma unroll
-        for (int j = 0; j < HALF_TOK; ++j) {
-          const int tok = half * HALF_TOK + j;
+        for (int j = 0; j < SLICE_TOK; ++j) {
+          const int tok = slice * SLICE_TOK + j;
           if (tok < ntok) {
             const float v = (key <= pos0 + tok) ? ks * acc[j] : -INFINITY;
             p.scores[static_cast<int64_t>(t0 + tok) * p.score_stride + key] = v;
@@ -319,11 +353,15 @@ smla_status_t launch_indexer(const uint8_t* q, const float* q_scale, const uint8
   const int64_t est_tt = (seqs.T + tok - 1) / tok;
   int64_t chunk = (est_tt * key_tiles + 2 * 152 - 1) / (2 * 152);
   chunk = std::max<int64_t>(1, std::min<int64_t>(chunk, key_tiles));
+  // the item's page ids are staged in shared memory (kMaxItemPages)
+  chunk = std::min<int64_t>(chunk, static_cast<int64_t>(kMaxItemPages - 2) * seqs.page_size / kBM);
+  chunk = std::max<int64_t>(1, chunk);
   const int64_t nchunk = (key_tiles + chunk - 1) / chunk;
   const int64_t grid = (est_tt + seqs.B) * nchunk;  // upper bound; CTAs past the last item exit at once
   if (grid > 0x7fffffff) return fail(SMLA_ERR_UNSUPPORTED, "indexer grid too large");
   Params p{q_scale, k_scale, phys_rows, seqs.cu_q, seqs.kv_len, seqs.page_table, seqs.B, seqs.max_pages,
-           seqs.page_size, seqs.T, scores, score_stride, static_cast<int>(chunk), box_rows, err};
+           seqs.page_size, seqs.T, __builtin_ctz(static_cast<unsigned>(seqs.page_size)), scores, score_stride,
+           static_cast<int>(chunk), box_rows, err};
   cudaError_t e;
   switch (h_idx) {
     case 4: e = launch_t<4>(tq, tk, p, static_cast<int>(grid), stream); break;
