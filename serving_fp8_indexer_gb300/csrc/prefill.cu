@@ -90,7 +90,7 @@ static_assert(kSoftThreads * kSoftRegs + (threads_for(1) - kSoftThreads) * kLowR
               "register split exceeds the launch allocation");
 static_assert(kSoftWarps % 4 == 0 && kMmaWarp % 4 == 0, "roles must split on warpgroup boundaries");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 256;  // S^T accumulators (64 columns each) from 256; O^T tiles at [0, 256)
+constexpr uint32_t kTmemS = 256;  // S^T accumulators from 256; O^T tiles at [0, 256)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTau = 8.0f;      // lazy-rescale threshold (log2 units)
 constexpr int kOrdMin = static_cast<int>(0x80000000u);
@@ -114,7 +114,9 @@ struct Params {
 
 template <int QP, int KVP, int PP, int NST>
 struct Smem {
-  uint8_t q[QP][kQBytes];
+  // Q as the QK B operand, [chunk][QP x 64 rows][64 B]: for bf16 q the hi
+  // rows 0..63 and lo rows 64..127 of a chunk are one 128-row operand
+  uint8_t q[QP * kQBytes];
   uint8_t kv[NST][KVP][kKVBytes];
   uint8_t plo[PP == 2 ? kChunkBytes : 16];  // P lo term (bf16 path)
   uint32_t idx[kBK];
@@ -164,26 +166,26 @@ __device__ __forceinline__ uint4 quant16(const float (&x)[16]) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Issues QK of one block: S^T[128 keys x 64 heads] over the 576 columns,
-// the MMAs rotating over NACC accumulators (MMA i of the block goes to
-// accumulator i % NACC; the first NACC overwrite).  Every operand offset is
-// a compile-time constant.
+// Issues QK of one block: S^T[128 keys x QP*64] over the 576 columns (for
+// bf16 q the hi and lo products side by side, one N = 128 MMA per K step, so
+// each key tile is read once for both), the MMAs rotating over NACC
+// accumulators (MMA i of the block goes to accumulator i % NACC; the first
+// NACC overwrite).  Every operand offset is a compile-time constant.
 template <int QP, int KVP, int NACC>
 __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t a0, uint64_t b0, uint32_t idesc) {
+  constexpr int kQN = QP * kNH;
 #pragma unroll
   for (int kc = 0; kc < kChunks; ++kc)
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
-      for (int qp = 0; qp < QP; ++qp)
-#pragma unroll
-        for (int kp = 0; kp < KVP; ++kp) {
-          const int i = ((kc * 2 + kk) * QP + qp) * KVP + kp;
-          // descriptor address fields are in 16-byte units: add offsets >> 4
-          const uint64_t ad = a0 + static_cast<uint64_t>((kp * kKVBytes + kc * kChunkBytes + kk * 32) >> 4);
-          const uint64_t bd = b0 + static_cast<uint64_t>((qp * kQBytes + kc * (kNH * 64) + kk * 32) >> 4);
-          mma_f8f6f4_ss(s_tmem + (i % NACC) * kNH, ad, bd, idesc, i < NACC ? 0u : 1u);
-        }
+      for (int kp = 0; kp < KVP; ++kp) {
+        const int i = (kc * 2 + kk) * KVP + kp;
+        // descriptor address fields are in 16-byte units: add offsets >> 4
+        const uint64_t ad = a0 + static_cast<uint64_t>((kp * kKVBytes + kc * kChunkBytes + kk * 32) >> 4);
+        const uint64_t bd = b0 + static_cast<uint64_t>((kc * kQN * 64 + kk * 32) >> 4);
+        mma_f8f6f4_ss(s_tmem + (i % NACC) * kQN, ad, bd, idesc, i < NACC ? 0u : 1u);
+      }
 }
 
 template <int QP, int KVP, int PP, int NST, int SC>
@@ -196,7 +198,9 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
   // its accumulator but not for other MMAs (measured: two alternating
   // accumulators already run a block's QK as fast as three).
   constexpr int kSAcc = 2;
-  static_assert(kTmemS + kNH * kSAcc <= kTmemCols, "TMEM budget");
+  constexpr int kQN = QP * kNH;  // QK MMA N
+  static_assert(kSAcc == 2, "the softmax sums exactly two S accumulators");
+  static_assert(kTmemS + kQN * kSAcc <= kTmemCols, "TMEM budget");
   constexpr int kThreads = threads_for(KVP);
   constexpr int kProdThreads = 32 * prod_warps(KVP);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -301,9 +305,9 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
           split16(x, hi, lo);
           const int e0 = qtr * 144 + 16 * i;
           const int kc = e0 >> 6, c4 = (e0 & 63) >> 4;
-          const uint32_t off = kc * (kNH * 64) + hh * 64 + sw64(hh, c4);
-          *reinterpret_cast<uint4*>(&s.q[0][off]) = hi;
-          *reinterpret_cast<uint4*>(&s.q[QP - 1][off]) = lo;
+          const uint32_t off = kc * (kQN * 64) + hh * 64 + sw64(hh, c4);
+          *reinterpret_cast<uint4*>(&s.q[off]) = hi;
+          *reinterpret_cast<uint4*>(&s.q[off + kNH * 64]) = lo;
         }
       } else {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) +
@@ -312,7 +316,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
           const uint4 v = hvalid ? ld_stream16(src + i) : make_uint4(0, 0, 0, 0);
           const int e0 = qtr * 144 + 16 * i;
           const int kc = e0 >> 6, c4 = (e0 & 63) >> 4;
-          *reinterpret_cast<uint4*>(&s.q[0][kc * (kNH * 64) + hh * 64 + sw64(hh, c4)]) = v;
+          *reinterpret_cast<uint4*>(&s.q[kc * (kQN * 64) + hh * 64 + sw64(hh, c4)]) = v;
         }
       }
       if (qtr == 0) {
@@ -341,17 +345,19 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
       tc_fence_after();
       float y[32];
       {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kTmemS + hb, v);
+        // S = sum of the kSAcc accumulators' QP term columns, two loads per wait
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tmem + lane_base + kTmemS + hb, v0);
+        tmem_ld32(tmem + lane_base + kTmemS + (QP == 2 ? kNH : kQN) + hb, v1);
         tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 32; ++h) y[h] = __uint_as_float(v[h]);
-#pragma unroll
-        for (int a = 1; a < kSAcc; ++a) {
-          tmem_ld32(tmem + lane_base + kTmemS + a * kNH + hb, v);
+        for (int h = 0; h < 32; ++h) y[h] = __uint_as_float(v0[h]) + __uint_as_float(v1[h]);
+        if (QP == 2) {
+          tmem_ld32(tmem + lane_base + kTmemS + kQN + hb, v0);
+          tmem_ld32(tmem + lane_base + kTmemS + kQN + kNH + hb, v1);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 32; ++h) y[h] += __uint_as_float(v[h]);
+          for (int h = 0; h < 32; ++h) y[h] += __uint_as_float(v0[h]) + __uint_as_float(v1[h]);
         }
       }
       tc_fence_before();
@@ -533,8 +539,8 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     // has released S.  The whole warp runs the loop; one elected lane issues.
     setmaxnreg_dec<kLowRegs>();
     const bool leader = elect_one();
-    constexpr uint32_t IDESC_QK = idesc_e4m3_f32(kBK, kNH, 0, 0);
-    const uint64_t qk_b0 = make_sdesc(smem_u32(s.q[0]), 16, 512, kSwizzle64B);
+    constexpr uint32_t IDESC_QK = idesc_e4m3_f32(kBK, kQN, 0, 0);
+    const uint64_t qk_b0 = make_sdesc(smem_u32(s.q), 16, 512, kSwizzle64B);
     const uint64_t kv_a0 = make_sdesc(smem_u32(s.kv[0][0]), 16, 512, kSwizzle64B);
     bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_q), 0, p.err));
     for (int j = 0; ok && j < nblk; ++j) {
