@@ -114,8 +114,9 @@ __device__ __forceinline__ void emit(const Params& p, int b, const int* ptab, ui
 
 // Finds the digit bin holding the krem-th largest candidate (bins counted
 // from the top), returns it and subtracts the count above it from krem.
+// *bin_count (if given) receives the bin's own count.
 __device__ __forceinline__ int select_bin(const uint32_t* hist, int& krem, int* warp_tot, int* sh_bin,
-                                          int* sh_above) {
+                                          int* sh_above, int* bin_count = nullptr) {
   const int tid = threadIdx.x;
   const int rt = kThreads - 1 - tid;  // thread rt owns bins [rt*4, rt*4+4)
   int local = 0;
@@ -130,6 +131,7 @@ __device__ __forceinline__ int select_bin(const uint32_t* hist, int& krem, int* 
     if (c < krem && c + h >= krem) {
       *sh_bin = bin;
       *sh_above = c;
+      if (bin_count) *bin_count = h;
     }
     c += h;
   }
@@ -138,6 +140,209 @@ __device__ __forceinline__ int select_bin(const uint32_t* hist, int& krem, int* 
   krem -= *sh_above;
   __syncthreads();
   return bin;
+}
+
+// Sequence b of token t (the number of sequence ends cu_q[b+1] <= t) and its
+// number of valid keys n = pos + 1; flags and clamps inconsistent shapes.
+__device__ __forceinline__ void token_row(const Params& p, int t, int* sh_b, int& b, int& n) {
+  const int tid = threadIdx.x;
+  if (tid < 32) {
+    int cnt = 0;
+    for (int b0 = 0; b0 < p.B; b0 += 32) {
+      const int bb = b0 + tid;
+      cnt += __popc(__ballot_sync(0xffffffffu, bb < p.B && p.cu_q[bb + 1] <= t));
+    }
+    if (tid == 0) *sh_b = min(cnt, p.B - 1);
+  }
+  __syncthreads();
+  b = *sh_b;
+  const int q_len = p.cu_q[b + 1] - p.cu_q[b];
+  const int kvl = p.kv_len[b];
+  n = kvl - q_len + (t - p.cu_q[b]) + 1;  // valid keys 0..pos
+  if (n < 1 || n > p.stride || kvl < q_len) {
+    if (tid == 0) atomicOr(p.err, kErrShape);
+    n = max(0, min(n, static_cast<int>(p.stride)));
+  }
+}
+
+// Register-resident selection for rows of at most 2048 * E4 keys: thread tid
+// holds the keys 4 * (e * 512 + tid) + u (e < E4, u < 4), read once as
+// float4.  11-bit digit histograms over the keys still matching the prefix
+// find the k-th largest ordered key (stopping early once the bin holding it
+// is taken whole); one compaction in key order (e, tid, u) then emits the
+// keys above it and the lowest-keyed krem of its ties, from per-warp prefix
+// sums of the two counts.
+template <int E4>
+__global__ void __launch_bounds__(kThreads, E4 <= 4 ? 3 : 1) topk_reg_kernel(const Params p) {
+  constexpr int E = 4 * E4;
+  __shared__ uint32_t hist[kBins];
+  __shared__ int warp_tot[kWarps + 1];
+  __shared__ uint32_t s_wmin[kWarps], s_wmax[kWarps];
+  __shared__ int gt_w[E4][kWarps], eq_w[E4][kWarps];
+  __shared__ int sh_b, sh_bin, sh_above, sh_cnt;
+
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int b, n;
+  token_row(p, t, &sh_b, b, n);
+  const int k = p.k;
+  uint32_t* out = p.indices + static_cast<int64_t>(t) * k;
+  if (n <= k) {
+    for (int key = tid; key < n; key += kThreads) out[key] = phys_row(p, b, key);
+    for (int i = n + tid; i < k; i += kThreads) out[i] = 0xFFFFFFFFu;
+    if (tid == 0) p.lens[t] = static_cast<uint32_t>(n);
+    return;
+  }
+  if (n > 2048 * E4) {  // the host picks E4 from the row stride; never taken
+    if (tid == 0) atomicOr(p.err, kErrShape);
+    return;
+  }
+  const float* row = p.scores + static_cast<int64_t>(t) * p.stride;
+  uint32_t u[E];
+  uint32_t kmin = 0xffffffffu, kmax = 0u;
+#pragma unroll
+  for (int e = 0; e < E4; ++e) {
+    const int key0 = 4 * (e * kThreads + tid);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (key0 + 3 < n) {
+      v = __ldcs(reinterpret_cast<const float4*>(row + key0));
+    } else if (key0 < n) {
+      v.x = row[key0];
+      if (key0 + 1 < n) v.y = row[key0 + 1];
+      if (key0 + 2 < n) v.z = row[key0 + 2];
+    }
+    const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      u[4 * e + q] = ordered(f[q]);
+      if (key0 + q < n) {
+        kmin = min(kmin, u[4 * e + q]);
+        kmax = max(kmax, u[4 * e + q]);
+      }
+    }
+  }
+  auto valid = [&](int i) { return 4 * ((i >> 2) * kThreads + tid) + (i & 3) < n; };
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) {
+    s_wmin[warp] = kmin;
+    s_wmax[warp] = kmax;
+  }
+  __syncthreads();
+  kmin = s_wmin[0];
+  kmax = s_wmax[0];
+#pragma unroll
+  for (int w = 1; w < kWarps; ++w) {
+    kmin = min(kmin, s_wmin[w]);
+    kmax = max(kmax, s_wmax[w]);
+  }
+  // ---- digits.  Keys matching (hi_mask, hi_val) are the candidates; krem of
+  // them are still to be taken.
+  int krem = k;
+  uint32_t hi_mask = 0xffffffffu, hi_val = kmax;  // all keys equal: every key ties kmax
+  bool whole = false;                             // the candidates are all taken
+  const uint32_t diff = kmin ^ kmax;
+  if (diff != 0) {
+    int top = 31 - __clz(diff);
+    hi_mask = top == 31 ? 0u : ~((2u << top) - 1u);
+    hi_val = kmax & hi_mask;
+    while (top >= 0) {
+      const int sh = max(0, top - 10);
+      const uint32_t dmask = (1u << (top - sh + 1)) - 1u;
+      for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < E; ++i)
+        if (valid(i) && (u[i] & hi_mask) == hi_val) atomicAdd(&hist[(u[i] >> sh) & dmask], 1u);
+      __syncthreads();
+      const int bin = select_bin(hist, krem, warp_tot, &sh_bin, &sh_above, &sh_cnt);
+      hi_val |= static_cast<uint32_t>(bin) << sh;
+      hi_mask |= dmask << sh;
+      top = sh - 1;
+      if (sh_cnt == krem) {  // uniform: read after the barrier inside select_bin
+        whole = true;
+        break;
+      }
+    }
+  }
+  // ---- compaction in key order.  gt: above the candidates' prefix (or a
+  // whole-taken candidate); eq: a candidate tie, taken while fewer than krem
+  // ties precede it.
+  int g_cnt[E4], e_cnt[E4];
+#pragma unroll
+  for (int e = 0; e < E4; ++e) {
+    int g = 0, q = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = 4 * e + j;
+      if (!valid(i)) continue;
+      const bool cand = (u[i] & hi_mask) == hi_val;
+      g += (u[i] > (hi_val | ~hi_mask) || (whole && cand)) ? 1 : 0;
+      q += (!whole && cand) ? 1 : 0;
+    }
+    // warp-exclusive prefix of g and q
+    int gi = g, qi = q;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, gi, o), c = __shfl_up_sync(0xffffffffu, qi, o);
+      if (lane >= o) {
+        gi += a;
+        qi += c;
+      }
+    }
+    if (lane == 31) {
+      gt_w[e][warp] = gi;
+      eq_w[e][warp] = qi;
+    }
+    g_cnt[e] = gi - g;
+    e_cnt[e] = qi - q;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive prefix over (e, warp) in key order: E4 * 16 entries, lane l takes entries l, l+32, ...
+    int run_g = 0, run_q = 0;
+    for (int base = 0; base < E4 * kWarps; base += 32) {
+      const int idx = base + lane;
+      const int g = idx < E4 * kWarps ? gt_w[idx / kWarps][idx % kWarps] : 0;
+      const int q = idx < E4 * kWarps ? eq_w[idx / kWarps][idx % kWarps] : 0;
+      int gi = g, qi = q;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int a = __shfl_up_sync(0xffffffffu, gi, o), c = __shfl_up_sync(0xffffffffu, qi, o);
+        if (lane >= o) {
+          gi += a;
+          qi += c;
+        }
+      }
+      __syncwarp();
+      if (idx < E4 * kWarps) {
+        gt_w[idx / kWarps][idx % kWarps] = run_g + gi - g;
+        eq_w[idx / kWarps][idx % kWarps] = run_q + qi - q;
+      }
+      run_g += __shfl_sync(0xffffffffu, gi, 31);
+      run_q += __shfl_sync(0xffffffffu, qi, 31);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < E4; ++e) {
+    int gb = gt_w[e][warp] + g_cnt[e], qb = eq_w[e][warp] + e_cnt[e];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = 4 * e + j;
+      if (!valid(i)) continue;
+      const int key = 4 * (e * kThreads + tid) + j;
+      const bool cand = (u[i] & hi_mask) == hi_val;
+      if (u[i] > (hi_val | ~hi_mask) || (whole && cand)) {
+        emit(p, b, nullptr, out, gb + min(qb, krem), key);
+        ++gb;
+      } else if (!whole && cand) {
+        if (qb < krem) emit(p, b, nullptr, out, gb + qb, key);
+        ++qb;
+      }
+    }
+  }
+  if (tid == 0) p.lens[t] = static_cast<uint32_t>(k);
 }
 
 __global__ void __launch_bounds__(kThreads, 3) topk_kernel(const Params p) {
@@ -400,7 +605,12 @@ smla_status_t launch_topk(const float* scores, int64_t score_stride, const smla_
   Params p{scores, score_stride, seqs.cu_q, seqs.kv_len, seqs.page_table, seqs.B, seqs.max_pages,
            seqs.page_size, seqs.T, __builtin_ctz(static_cast<unsigned>(seqs.page_size)), k, indices, topk_lengths,
            static_cast<int>(cap), static_cast<int>(cand_cap), static_cast<int>(pt_cap), err};
-  topk_kernel<<<seqs.T, kThreads, smem, stream>>>(p);
+  if (score_stride <= 2048 * 4)
+    topk_reg_kernel<4><<<seqs.T, kThreads, 0, stream>>>(p);
+  else if (score_stride <= 2048 * 8)
+    topk_reg_kernel<8><<<seqs.T, kThreads, 0, stream>>>(p);
+  else
+    topk_kernel<<<seqs.T, kThreads, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, "topk launch");
   return SMLA_OK;

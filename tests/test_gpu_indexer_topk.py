@@ -4,6 +4,7 @@ import numpy as np
 import pytest
 import torch
 
+import serving_fp8_indexer_gb300 as smla
 from serving_fp8_indexer_gb300 import workloads as wl
 
 from _gpu_helpers import (check_scores, check_topk_against, run_indexer, run_topk, sample_tokens,
@@ -102,3 +103,37 @@ def test_e2e_chunk_indexer_topk_full_size_sampled():
     # every token: the length rule and a filled tail
     pos = wl.token_positions(w.seqs)
     assert np.array_equal(lens.cpu().numpy(), np.minimum(pos + 1, w.topk).astype(np.uint32))
+
+
+@pytest.mark.parametrize("stride", [8192, 12288, 20000])
+@pytest.mark.parametrize("dist", ["normal", "ties", "equal"])
+def test_topk_paths_on_synthetic_rows(stride, dist):
+    """Top-k alone on controlled score rows: each stride picks one kernel path
+    (register rows of 16 or 32 keys a thread, or the shared-memory row cache);
+    the distributions exercise plain selection, long runs of ties at the k-th
+    value (the lowest keys win) and rows whose valid scores are all equal."""
+    L = stride - 37
+    w = wl.build("topk_paths", 50 + stride % 97, [6], [L], 64, h_idx=4, topk=2048)
+    rng = np.random.default_rng(stride)
+    pos = wl.token_positions(w.seqs)
+    rows = np.full((w.seqs.T, stride), -np.inf, dtype=np.float32)
+    for t in range(w.seqs.T):
+        n = int(pos[t]) + 1
+        if dist == "normal":
+            rows[t, :n] = rng.standard_normal(n).astype(np.float32)
+        elif dist == "ties":
+            rows[t, :n] = rng.integers(0, 4, size=n).astype(np.float32)
+        else:
+            rows[t, :n] = 1.5
+    seqs = smla.Seqs.from_host(w.seqs, "cuda")
+    scores = torch.from_numpy(rows).cuda()
+    idx, lens = run_topk(seqs, scores, w.topk, w.seqs.T)
+    gi, gl = idx.cpu().numpy(), lens.cpu().numpy()
+    toks = np.arange(w.seqs.T)
+    check_topk_against(w, rows.astype(np.float64), gi, gl, toks, w.topk, exact=True)
+    # selected keys come out in ascending logical-key order
+    for t in toks:
+        g = gi[t, :int(gl[t])].astype(np.int64)
+        lk = {int(r): j for j, r in enumerate(wl.logical_to_phys(w.seqs, 0, np.arange(int(pos[t]) + 1)))}
+        order = [lk[int(r)] for r in g]
+        assert order == sorted(order), f"token {t}: output not in key order"
