@@ -157,6 +157,22 @@ __device__ __forceinline__ void split16(const float (&x)[16], uint4& hi, uint4& 
   hi = make_uint4(h[0], h[1], h[2], h[3]);
   lo = make_uint4(l[0], l[1], l[2], l[3]);
 }
+// The same split for 8 floats into two 8-byte halves of a chunk.
+__device__ __forceinline__ void split8(const float (&x)[8], uint2& hi, uint2& lo) {
+  uint32_t h[2], l[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t a = f32x2_to_f16x2(x[4 * i + 0], x[4 * i + 1]);
+    const uint32_t b = f32x2_to_f16x2(x[4 * i + 2], x[4 * i + 3]);
+    const uint16_t ha = f16x2_to_e4m3x2(a), hb = f16x2_to_e4m3x2(b);
+    const uint16_t la = f16x2_to_e4m3x2(hsub2(a, e4m3x2_to_f16x2(ha)));
+    const uint16_t lb = f16x2_to_e4m3x2(hsub2(b, e4m3x2_to_f16x2(hb)));
+    h[i] = static_cast<uint32_t>(ha) | (static_cast<uint32_t>(hb) << 16);
+    l[i] = static_cast<uint32_t>(la) | (static_cast<uint32_t>(lb) << 16);
+  }
+  hi = make_uint2(h[0], h[1]);
+  lo = make_uint2(l[0], l[1]);
+}
 __device__ __forceinline__ uint4 quant16(const float (&x)[16]) {
   uint32_t w[4];
 #pragma unroll
@@ -188,6 +204,49 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t a0, uint64_t 
       }
 }
 
+// One work item: a token and one group of 64 heads.
+struct Item {
+  int t, h0, hv, n, nblk;
+};
+__device__ __forceinline__ Item item_at(const Params& p, int w, int groups) {
+  Item it;
+  it.t = w / groups;
+  it.h0 = (w % groups) * kNH;
+  it.hv = min(kNH, p.H - it.h0);
+  int n = static_cast<int>(p.lens[it.t]);
+  if (n > p.indices_stride) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrShape);
+    n = p.indices_stride;
+  }
+  it.n = n;
+  it.nblk = (n + kBK - 1) / kBK;
+  return it;
+}
+
+// 8 x 8 transpose across the 8-lane groups of a warp: lane m of a group
+// holding e[i] = X[m][i] ends with e[i] = X[i][m].
+__device__ __forceinline__ void transpose8(float (&e)[8], int lane) {
+#pragma unroll
+  for (int sft = 1; sft < 8; sft <<= 1) {
+    const bool up = (lane & sft) != 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i & sft) continue;
+      const float send = up ? e[i] : e[i | sft];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, sft);
+      if (up)
+        e[i] = recv;
+      else
+        e[i | sft] = recv;
+    }
+  }
+}
+
+// Persistent CTAs: CTA c takes the work items c, c + gridDim.x, ... in turn,
+// and every pipeline barrier keeps counting across items (a block's slot and
+// phases come from its index g over all of this CTA's blocks), so the next
+// item's first rows are gathered, and its q split, while the current item's
+// last blocks and epilogue run.
 template <int QP, int KVP, int PP, int NST, int SC>
 __global__ void __launch_bounds__(threads_for(KVP), 1)
     prefill_kernel(const Params p) {
@@ -212,22 +271,8 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     return;
   }
   S& s = *reinterpret_cast<S*>(smem_raw);
-  const int t = blockIdx.x;
-  const int h0 = blockIdx.y * kNH;
-  const int hv = min(kNH, p.H - h0);  // valid heads of this CTA
-  int n = static_cast<int>(p.lens[t]);
-  if (n > p.indices_stride) {
-    if (threadIdx.x == 0) atomicOr(p.err, kErrShape);
-    n = p.indices_stride;
-  }
-  const int nblk = (n + kBK - 1) / kBK;
-  const uint32_t* tok_idx = p.indices + static_cast<int64_t>(t) * p.indices_stride;
-  uint16_t* out_t = p.out + (static_cast<int64_t>(t) * p.H + h0) * kDV;
-
-  if (n == 0) {  // empty selection: zeros (no softmax mass)
-    for (int i = threadIdx.x; i < hv * kDV / 8; i += kThreads) __stcs(reinterpret_cast<uint4*>(out_t) + i, make_uint4(0, 0, 0, 0));
-    return;
-  }
+  const int groups = (p.H + kNH - 1) / kNH;
+  const int items = p.T * groups;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&s.bar_q), kSoftThreads);
@@ -258,32 +303,35 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     const int half = warp >> 2;             // heads [32*half, 32*half + 32)
     const int hb = half * 32;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    // ---- Q: 4 threads per head, 144 elements each, as 9 groups of 16
-    {
+    // ---- q of item w into s.q (its QK B operand) and its scales into s.cs:
+    // 4 threads per head, 144 elements each, all loads in flight at once;
+    // bf16 q is split into e4m3 hi + lo with a per-head power of two that
+    // puts the largest |q| * 2^e in [128, 256).  Called once s.q is free
+    // (before the first item, then after an item's last block, whose
+    // softmax started only after its QK completed).
+    auto load_q = [&](int w) {
+      const Item I = item_at(p, w, groups);
       const int hh = threadIdx.x >> 2, qtr = threadIdx.x & 3;
-      const bool hvalid = hh < hv;
+      const bool hvalid = hh < I.hv;
+      const int64_t qrow = static_cast<int64_t>(I.t) * p.H + I.h0 + hh;
       float sigma = 1.f;
       if (QP == 2) {
-        // one pass: the thread's 144 bf16 values stay in registers between
-        // the head maximum and the split
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) +
-                                                          (static_cast<int64_t>(t) * p.H + h0 + hh) * kD + qtr * 144);
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + qrow * kD + qtr * 144);
         uint4 v[18];
 #pragma unroll
         for (int i = 0; i < 18; ++i) v[i] = hvalid ? ld_stream16(src + i) : make_uint4(0, 0, 0, 0);
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 18; ++i) {
-          const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+          const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            amax = fmaxf(amax, fabsf(__uint_as_float(w[k] << 16)));
-            amax = fmaxf(amax, fabsf(__uint_as_float(w[k] & 0xffff0000u)));
+            amax = fmaxf(amax, fabsf(__uint_as_float(wv[k] << 16)));
+            amax = fmaxf(amax, fabsf(__uint_as_float(wv[k] & 0xffff0000u)));
           }
         }
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        // scale so that the largest |q| * 2^e lies in [128, 256)
         int e = 0;
         if (amax > 0.f) {
           int ex;
@@ -294,12 +342,12 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
 #pragma unroll
         for (int i = 0; i < 9; ++i) {
           float x[16];
-          const uint32_t w[8] = {v[2 * i].x, v[2 * i].y, v[2 * i].z, v[2 * i].w,
-                                 v[2 * i + 1].x, v[2 * i + 1].y, v[2 * i + 1].z, v[2 * i + 1].w};
+          const uint32_t wv[8] = {v[2 * i].x, v[2 * i].y, v[2 * i].z, v[2 * i].w,
+                                  v[2 * i + 1].x, v[2 * i + 1].y, v[2 * i + 1].z, v[2 * i + 1].w};
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            x[2 * k] = __uint_as_float(w[k] << 16) * sigma;
-            x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u) * sigma;
+            x[2 * k] = __uint_as_float(wv[k] << 16) * sigma;
+            x[2 * k + 1] = __uint_as_float(wv[k] & 0xffff0000u) * sigma;
           }
           uint4 hi, lo;
           split16(x, hi, lo);
@@ -310,8 +358,8 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
           *reinterpret_cast<uint4*>(&s.q[off + kNH * 64]) = lo;
         }
       } else {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) +
-                                                          (static_cast<int64_t>(t) * p.H + h0 + hh) * kD + qtr * 144);
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) + qrow * kD + qtr * 144);
+#pragma unroll
         for (int i = 0; i < 9; ++i) {
           const uint4 v = hvalid ? ld_stream16(src + i) : make_uint4(0, 0, 0, 0);
           const int e0 = qtr * 144 + 16 * i;
@@ -319,379 +367,435 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
           *reinterpret_cast<uint4*>(&s.q[kc * (kQN * 64) + hh * 64 + sw64(hh, c4)]) = v;
         }
       }
-      if (qtr == 0) {
-        s.cs[hh] = p.softmax_scale * kLog2e / sigma;
-        s.negm[hh] = 0.f;  // block 0 sets the reference
-      }
+      if (qtr == 0) s.cs[hh] = p.softmax_scale * kLog2e / sigma;
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&s.bar_q));
-    }
-    named_bar_sync(1, kSoftThreads);
-
-    // lv[h]: this key lane's share of head hb+h's softmax denominator, summed
-    // over the blocks (P / s_row, in the current reference's units)
-    float lv[32];
-#pragma unroll
-    for (int h = 0; h < 32; ++h) lv[h] = 0.f;
+    };
+    // the next item after w that has keys (items past the end: none)
+    auto next_nonempty = [&](int w) {
+      for (w += gridDim.x; w < items; w += gridDim.x)
+        if (item_at(p, w, groups).n > 0) return w;
+      return items;
+    };
+    int gb = 0;  // index of the item's first block among this CTA's blocks
     bool ok = true;
-
-    for (int j = 0; ok && j < nblk; ++j) {
-      const int slot = j % NST;
-      // S^T of block j is ready; kv_full is also waited so that the
-      // producers' per-row scales are visible to this thread.
-      bool w = mbar_wait(smem_u32(&s.bar_s_full), j & 1, p.err) &&
-               mbar_wait(smem_u32(&s.bar_kv_full[slot]), (j / NST) & 1, p.err);
-      if (!named_bar_and(1, kSoftThreads, w)) { ok = false; break; }
-      tc_fence_after();
-      float y[32];
-      {
-        // S = sum of the kSAcc accumulators' QP term columns, two loads per wait
-        uint32_t v0[32], v1[32];
-        tmem_ld32(tmem + lane_base + kTmemS + hb, v0);
-        tmem_ld32(tmem + lane_base + kTmemS + (QP == 2 ? kNH : kQN) + hb, v1);
-        tmem_wait_ld();
+    {
+      const int w0 = blockIdx.x < items && item_at(p, blockIdx.x, groups).n > 0 ? static_cast<int>(blockIdx.x)
+                                                                                  : next_nonempty(blockIdx.x);
+      if (w0 < items) load_q(w0);
+    }
+    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
+      const Item I = item_at(p, w, groups);
+      const int n = I.n, nblk = I.nblk;
+      uint16_t* out_t = p.out + (static_cast<int64_t>(I.t) * p.H + I.h0) * kDV;
+      if (n == 0) {  // empty selection: zeros (no softmax mass)
+        for (int i = threadIdx.x; i < I.hv * kDV / 8; i += kSoftThreads)
+          __stcs(reinterpret_cast<uint4*>(out_t) + i, make_uint4(0, 0, 0, 0));
+        continue;
+      }
+      if (threadIdx.x < kNH) s.negm[threadIdx.x] = 0.f;  // block 0 sets the reference
+      named_bar_sync(1, kSoftThreads);
+      // lv[h]: this key lane's share of head hb+h's softmax denominator,
+      // summed over the blocks (P / s_row, in the current reference's units)
+      float lv[32];
 #pragma unroll
-        for (int h = 0; h < 32; ++h) y[h] = __uint_as_float(v0[h]) + __uint_as_float(v1[h]);
-        if (QP == 2) {
-          tmem_ld32(tmem + lane_base + kTmemS + kQN + hb, v0);
-          tmem_ld32(tmem + lane_base + kTmemS + kQN + kNH + hb, v1);
+      for (int h = 0; h < 32; ++h) lv[h] = 0.f;
+
+      for (int j = 0; j < nblk; ++j) {
+        const int g = gb + j;
+        const int slot = g % NST;
+        // S^T of block j is ready; kv_full is also waited so that the
+        // producers' per-row scales are visible to this thread.
+        bool wt = mbar_wait(smem_u32(&s.bar_s_full), g & 1, p.err) &&
+                  mbar_wait(smem_u32(&s.bar_kv_full[slot]), (g / NST) & 1, p.err);
+        if (!named_bar_and(1, kSoftThreads, wt)) { ok = false; break; }
+        tc_fence_after();
+        float y[32];
+        {
+          // S = sum of the two accumulators' QP term columns, two loads per wait
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tmem + lane_base + kTmemS + hb, v0);
+          tmem_ld32(tmem + lane_base + kTmemS + (QP == 2 ? kNH : kQN) + hb, v1);
           tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 32; ++h) y[h] += __uint_as_float(v0[h]) + __uint_as_float(v1[h]);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&s.bar_s_free));  // S may now be overwritten by QK of block j+1
-      const float sr = SC == kUnit ? 1.f : s.srow[slot][r];
-      const float lg = SC == kUnit ? 0.f : __log2f(sr);
-      // y = logit (log2 units) minus the head's reference maximum m_h,
-      //   y = S * s_row * c_h - m_h,
-      // and the PV operand is exp2(y + log2 s_row).  Block 0 has m = 0: it
-      // computes the logits themselves and sets the references to its maxima.
-      float ymax = -INFINITY;
-      {
-        const float4* c4p = reinterpret_cast<const float4*>(s.cs + hb);
-        const float4* m4p = reinterpret_cast<const float4*>(s.negm + hb);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float4 c = c4p[q], m = m4p[q];
-          const float cc[4] = {c.x, c.y, c.z, c.w}, mm[4] = {m.x, m.y, m.z, m.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int h = 4 * q + k;
-            y[h] = fmaf(y[h], SC == kUnit ? cc[k] : sr * cc[k], mm[k]);
-            ymax = fmaxf(ymax, y[h]);
-          }
-        }
-      }
-      if ((j + 1) * kBK > n && j * kBK + r >= n) {  // lanes past the selection (last block only)
-#pragma unroll
-        for (int h = 0; h < 32; ++h) y[h] = -INFINITY;
-        ymax = -INFINITY;
-      }
-      // Fast path: no element exceeds its head's reference by more than tau.
-      if (named_bar_or(1, kSoftThreads, j == 0 || ymax + lg > kTau)) {
-        // Slow path (always taken by block 0): t_h = block maximum of y + lg
-        // per head across the 128 key lanes.  Block 0 sets m_h = t_h; a
-        // later block raises m_h by t_h where t_h > tau and scales O^T and
-        // the row sums of that head by exp2(-t_h).
-        int mine = kOrdMin;
-#pragma unroll
-        for (int h = 0; h < 32; ++h) {
-          const int m = __reduce_max_sync(0xffffffffu, ord_int(y[h] + lg));
-          if (lane == h) mine = m;
-        }
-        atomicMax(&s.mx[hb + lane], mine);
-        named_bar_sync(1, kSoftThreads);
-        if ((warp & 3) == 0) {
-          const int hh = hb + lane;
-          const float t = ord_float(s.mx[hh]);
-          s.mx[hh] = kOrdMin;
-          float d = 0.f, f = 1.f;
-          if (j == 0 || t > kTau) {
-            d = t;
-            if (j > 0) f = exp2f(-t);
-            s.negm[hh] -= t;
-          }
-          s.delta[hh] = d;
-          s.fac[hh] = f;
-        }
-        named_bar_sync(1, kSoftThreads);
-#pragma unroll
-        for (int h = 0; h < 32; ++h) y[h] -= s.delta[hb + h];
-        if (j > 0) {
-#pragma unroll
-          for (int h = 0; h < 32; ++h) lv[h] *= s.fac[hb + h];
-          // O^T holds blocks < j: wait for the last PV, then scale each head's column.
-          w = mbar_wait(smem_u32(&s.bar_pv_done), (j - 1) & 1, p.err);
-          if (!named_bar_and(1, kSoftThreads, w)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll 1
-          for (int part = 0; part < 8; ++part) {  // 4 tiles x 2 halves of this warp's 32 heads
-            uint32_t v[16];
-            const int c0 = (part & 1) * 16;
-            const uint32_t a = tmem + lane_base + (part >> 1) * kNH + hb + c0;
-            tmem_ld16(a, v);
+          for (int h = 0; h < 32; ++h) y[h] = __uint_as_float(v0[h]) + __uint_as_float(v1[h]);
+          if (QP == 2) {
+            tmem_ld32(tmem + lane_base + kTmemS + kQN + hb, v0);
+            tmem_ld32(tmem + lane_base + kTmemS + kQN + kNH + hb, v1);
             tmem_wait_ld();
 #pragma unroll
-            for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * s.fac[hb + c0 + h]);
-            tmem_st16(a, v);
+            for (int h = 0; h < 32; ++h) y[h] += __uint_as_float(v0[h]) + __uint_as_float(v1[h]);
           }
-          tmem_wait_st();
-          tc_fence_before();
         }
-      }
-      // ---- P row r (this thread's 32 heads) and the row sums
-      const float isr = 1.f / sr;
-      uint8_t* p_hi = &s.kv[slot][0][kRope * kChunkBytes];
-      uint4 lo_keep[2];
+        tc_fence_before();
+        mbar_arrive(smem_u32(&s.bar_s_free));  // S may now be overwritten by the next QK
+        const float sr = SC == kUnit ? 1.f : s.srow[slot][r];
+        const float lg = SC == kUnit ? 0.f : __log2f(sr);
+        // y = logit (log2 units) minus the head's reference maximum m_h,
+        //   y = S * s_row * c_h - m_h,
+        // and the PV operand is exp2(y + log2 s_row).  Block 0 has m = 0: it
+        // computes the logits themselves and sets the references to its maxima.
+        float ymax = -INFINITY;
+        {
+          const float4* c4p = reinterpret_cast<const float4*>(s.cs + hb);
+          const float4* m4p = reinterpret_cast<const float4*>(s.negm + hb);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float x[16];
+          for (int q = 0; q < 8; ++q) {
+            const float4 c = c4p[q], m = m4p[q];
+            const float cc[4] = {c.x, c.y, c.z, c.w}, mm[4] = {m.x, m.y, m.z, m.w};
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int h = c * 16 + k;
-          x[k] = ex2_approx(SC == kUnit ? y[h] : y[h] + lg);  // 0 past the selection
-          lv[h] = SC == kUnit ? lv[h] + x[k] : fmaf(x[k], isr, lv[h]);
+            for (int k = 0; k < 4; ++k) {
+              const int h = 4 * q + k;
+              y[h] = fmaf(y[h], SC == kUnit ? cc[k] : sr * cc[k], mm[k]);
+              ymax = fmaxf(ymax, y[h]);
+            }
+          }
         }
-        const int c4 = half * 2 + c;
-        if (PP == 2) {
-          uint4 hi;
-          split16(x, hi, lo_keep[c]);
-          *reinterpret_cast<uint4*>(p_hi + r * 64 + sw64(r, c4)) = hi;
-        } else {
-          *reinterpret_cast<uint4*>(p_hi + r * 64 + sw64(r, c4)) = quant16(x);
+        if ((j + 1) * kBK > n && j * kBK + r >= n) {  // lanes past the selection (last block only)
+#pragma unroll
+          for (int h = 0; h < 32; ++h) y[h] = -INFINITY;
+          ymax = -INFINITY;
         }
-      }
-      // PV of block j-1 must have completed: the single P-lo buffer is read by
-      // it, and P of block j is only published once the MMA warp has issued
-      // PV j-1 (so p_full never runs a phase ahead of its consumer).
-      if (j > 0) {
-        w = mbar_wait(smem_u32(&s.bar_pv_done), (j - 1) & 1, p.err);
-        if (!named_bar_and(1, kSoftThreads, w)) { ok = false; break; }
-      }
-      if (PP == 2) {
+        // Fast path: no element exceeds its head's reference by more than tau.
+        if (named_bar_or(1, kSoftThreads, j == 0 || ymax + lg > kTau)) {
+          // Slow path (always taken by block 0): t_h = block maximum of y + lg
+          // per head across the 128 key lanes.  Block 0 sets m_h = t_h; a
+          // later block raises m_h by t_h where t_h > tau and scales O^T and
+          // the row sums of that head by exp2(-t_h).
+          int mine = kOrdMin;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) *reinterpret_cast<uint4*>(s.plo + r * 64 + sw64(r, half * 2 + c)) = lo_keep[c];
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&s.bar_p_full));
-    }
-
-    // ---- row sums across the 128 key lanes, then O^T / l -> bf16.  The
-    // output rows of this CTA's heads are contiguous in `out`, so they are
-    // staged in shared memory (slot 0 is dead once the last PV completed)
-    // and written with one bulk copy.
-    const bool done =
-        named_bar_and(1, kSoftThreads, ok && mbar_wait(smem_u32(&s.bar_pv_done), (nblk - 1) & 1, p.err));
-    // dead slot 0: [64 heads][512] bf16 output stage, then the row-sum partials
-    uint16_t* stage = reinterpret_cast<uint16_t*>(s.kv[0][0]);
-    float(*lpart)[kNH] = reinterpret_cast<float(*)[kNH]>(s.kv[0][0] + kNH * kDV * 2);
-    static_assert(kNH * kDV * 2 + 4 * kNH * 4 <= kKVBytes, "epilogue scratch fits in a slot");
-    {
-      // Transpose-reduce: after log2(32) halving exchanges (31 shuffles),
-      // lane l holds the sum over the warp's 32 key lanes for head hb + l.
+          for (int h = 0; h < 32; ++h) {
+            const int m = __reduce_max_sync(0xffffffffu, ord_int(y[h] + lg));
+            if (lane == h) mine = m;
+          }
+          atomicMax(&s.mx[hb + lane], mine);
+          named_bar_sync(1, kSoftThreads);
+          if ((warp & 3) == 0) {
+            const int hh = hb + lane;
+            const float t = ord_float(s.mx[hh]);
+            s.mx[hh] = kOrdMin;
+            float d = 0.f, f = 1.f;
+            if (j == 0 || t > kTau) {
+              d = t;
+              if (j > 0) f = exp2f(-t);
+              s.negm[hh] -= t;
+            }
+            s.delta[hh] = d;
+            s.fac[hh] = f;
+          }
+          named_bar_sync(1, kSoftThreads);
 #pragma unroll
-      for (int step = 16; step >= 1; step >>= 1) {
-        const bool upper = (lane & step) != 0;
+          for (int h = 0; h < 32; ++h) y[h] -= s.delta[hb + h];
+          if (j > 0) {
 #pragma unroll
-        for (int i = 0; i < step; ++i) {
-          const float send = upper ? lv[i] : lv[i + step];
-          const float keep = upper ? lv[i + step] : lv[i];
-          lv[i] = keep + __shfl_xor_sync(0xffffffffu, send, step);
-        }
-      }
-      lpart[warp & 3][hb + lane] = lv[0];
-    }
-    named_bar_sync(1, kSoftThreads);
-    float* linv = s.fac;  // reused: 1 / row sum per head
-    if (threadIdx.x < kNH) {
-      const float l = lpart[0][threadIdx.x] + lpart[1][threadIdx.x] + lpart[2][threadIdx.x] + lpart[3][threadIdx.x];
-      linv[threadIdx.x] = l > 0.f ? 1.f / l : 0.f;
-    }
-    named_bar_sync(1, kSoftThreads);
-    if (done) {
-      tc_fence_after();
-      float inv[32];
-#pragma unroll
-      for (int h = 0; h < 32; ++h) inv[h] = linv[hb + h];
+            for (int h = 0; h < 32; ++h) lv[h] *= s.fac[hb + h];
+            // O^T holds blocks < j: wait for the last PV, then scale each head's column.
+            wt = mbar_wait(smem_u32(&s.bar_pv_done), (g - 1) & 1, p.err);
+            if (!named_bar_and(1, kSoftThreads, wt)) { ok = false; break; }
+            tc_fence_after();
 #pragma unroll 1
-      for (int tile = 0; tile < 4; ++tile) {
-        const int vcol = tile * 128 + r;
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_base + tile * kNH + hb, v);
-        tmem_wait_ld();
+            for (int part = 0; part < 8; ++part) {  // 4 tiles x 2 halves of this warp's 32 heads
+              uint32_t v[16];
+              const int c0 = (part & 1) * 16;
+              const uint32_t a = tmem + lane_base + (part >> 1) * kNH + hb + c0;
+              tmem_ld16(a, v);
+              tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 32; ++h)
-          stage[(hb + h) * kDV + vcol] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[h]) * inv[h]));
+              for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * s.fac[hb + c0 + h]);
+              tmem_st16(a, v);
+            }
+            tmem_wait_st();
+          }
+        }
+        // ---- P row r (this thread's 32 heads) and the row sums
+        const float isr = 1.f / sr;
+        uint8_t* p_hi = &s.kv[slot][0][kRope * kChunkBytes];
+        uint4 lo_keep[2];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float x[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int h = c * 16 + k;
+            x[k] = ex2_approx(SC == kUnit ? y[h] : y[h] + lg);  // 0 past the selection
+            lv[h] = SC == kUnit ? lv[h] + x[k] : fmaf(x[k], isr, lv[h]);
+          }
+          const int c4 = half * 2 + c;
+          if (PP == 2) {
+            uint4 hi;
+            split16(x, hi, lo_keep[c]);
+            *reinterpret_cast<uint4*>(p_hi + r * 64 + sw64(r, c4)) = hi;
+          } else {
+            *reinterpret_cast<uint4*>(p_hi + r * 64 + sw64(r, c4)) = quant16(x);
+          }
+        }
+        // PV of the previous block (possibly the previous item's last) must
+        // have completed: the single P-lo buffer is read by it, and P of this
+        // block is only published once that PV was issued (so p_full never
+        // runs a phase ahead of its consumer).
+        if (g > 0) {
+          wt = mbar_wait(smem_u32(&s.bar_pv_done), (g - 1) & 1, p.err);
+          if (!named_bar_and(1, kSoftThreads, wt)) { ok = false; break; }
+        }
+        if (PP == 2) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) *reinterpret_cast<uint4*>(s.plo + r * 64 + sw64(r, half * 2 + c)) = lo_keep[c];
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();  // this thread's TMEM reads (S; the epilogue's O) precede the PV it releases
+        mbar_arrive(smem_u32(&s.bar_p_full));
       }
-      fence_proxy_async_smem();
-    }
-    named_bar_sync(1, kSoftThreads);
-    if (done && threadIdx.x == 0) {
-      bulk_store_s2g(out_t, smem_u32(s.kv[0][0]), static_cast<uint32_t>(hv) * kDV * 2);
-      bulk_commit();
-      bulk_wait_read_all();  // the shared-memory source stays live until the copy has read it
+      if (!ok) break;
+      gb += nblk;
+
+      // ---- epilogue: row sums across the 128 key lanes (no PV needed yet)
+      float* linv = s.fac;  // reused: row sums, then 1 / row sum per head
+      if (threadIdx.x < kNH) linv[threadIdx.x] = 0.f;
+      named_bar_sync(1, kSoftThreads);
+      {
+        // Transpose-reduce: after log2(32) halving exchanges (31 shuffles),
+        // lane l holds the sum over the warp's 32 key lanes for head hb + l.
+#pragma unroll
+        for (int step = 16; step >= 1; step >>= 1) {
+          const bool upper = (lane & step) != 0;
+#pragma unroll
+          for (int i = 0; i < step; ++i) {
+            const float send = upper ? lv[i] : lv[i + step];
+            const float keep = upper ? lv[i + step] : lv[i];
+            lv[i] = keep + __shfl_xor_sync(0xffffffffu, send, step);
+          }
+        }
+        atomicAdd(&linv[hb + lane], lv[0]);
+      }
+      // the next item's q while this item's last PV runs (its QK is done),
+      // so the next QK overlaps this epilogue
+      {
+        const int wn = next_nonempty(w);
+        if (wn < items) load_q(wn);
+      }
+      // ---- O^T / l -> bf16 once the last PV has completed
+      const bool done = named_bar_and(1, kSoftThreads, mbar_wait(smem_u32(&s.bar_pv_done), (gb - 1) & 1, p.err));
+      if (threadIdx.x < kNH) {
+        const float l = linv[threadIdx.x];
+        linv[threadIdx.x] = l > 0.f ? 1.f / l : 0.f;
+      }
+      named_bar_sync(1, kSoftThreads);
+      if (done) {
+        tc_fence_after();
+        // Each 8-lane group transposes 8 heads x 8 columns, so a lane writes
+        // 8 consecutive bf16 of one head (16 bytes) straight to `out`.
+#pragma unroll 1
+        for (int tile = 0; tile < 4; ++tile) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + tile * kNH + hb, v);
+          tmem_wait_ld();
+          const int vcol0 = tile * 128 + (warp & 3) * 32 + 8 * (lane >> 3);
+#pragma unroll
+          for (int rd = 0; rd < 4; ++rd) {
+            float e[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) e[i] = __uint_as_float(v[8 * rd + i]);
+            transpose8(e, lane);
+            const int head = hb + 8 * rd + (lane & 7);
+            const float inv = linv[head];
+            uint4 o;
+            o.x = pack_bf16x2(e[0] * inv, e[1] * inv);
+            o.y = pack_bf16x2(e[2] * inv, e[3] * inv);
+            o.z = pack_bf16x2(e[4] * inv, e[5] * inv);
+            o.w = pack_bf16x2(e[6] * inv, e[7] * inv);
+            if (head < I.hv) __stcs(reinterpret_cast<uint4*>(out_t + static_cast<int64_t>(head) * kDV + vcol0), o);
+          }
+        }
+      }
+      // linv (s.fac) is rewritten by the next item's slow path only after the
+      // named barrier at that item's start; every thread has read it by then
     }
   } else if (warp == kMmaWarp) {
     // =================================================================== QK issuer
-    // QK of block j once its rows have landed and the softmax of block j-1
-    // has released S.  The whole warp runs the loop; one elected lane issues.
+    // QK of block g once its rows have landed, its item's q is in place and
+    // the softmax of block g-1 has released S.  The whole warp runs the loop;
+    // one elected lane issues.
     setmaxnreg_dec<kLowRegs>();
     const bool leader = elect_one();
     constexpr uint32_t IDESC_QK = idesc_e4m3_f32(kBK, kQN, 0, 0);
     const uint64_t qk_b0 = make_sdesc(smem_u32(s.q), 16, 512, kSwizzle64B);
     const uint64_t kv_a0 = make_sdesc(smem_u32(s.kv[0][0]), 16, 512, kSwizzle64B);
-    bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_q), 0, p.err));
-    for (int j = 0; ok && j < nblk; ++j) {
-      const bool w = (j == 0 || mbar_wait(smem_u32(&s.bar_s_free), (j - 1) & 1, p.err)) &&
-                     mbar_wait(smem_u32(&s.bar_kv_full[j % NST]), (j / NST) & 1, p.err);
-      if (!__all_sync(0xffffffffu, w)) break;
-      tc_fence_after();  // after the softmax's tcgen05.ld of S
-      const uint64_t slot_off = static_cast<uint64_t>(((j % NST) * KVP * kKVBytes) >> 4);
-      if (leader) {
-        issue_qk<QP, KVP, kSAcc>(tmem + kTmemS, kv_a0 + slot_off, qk_b0, IDESC_QK);
-        mma_commit(smem_u32(&s.bar_s_full));
+    int qn = 0, gb = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
+      const Item I = item_at(p, w, groups);
+      if (I.n == 0) continue;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_q), qn & 1, p.err));
+      ++qn;
+      for (int j = 0; ok && j < I.nblk; ++j) {
+        const int g = gb + j;
+        const bool wt = (g == 0 || mbar_wait(smem_u32(&s.bar_s_free), (g - 1) & 1, p.err)) &&
+                        mbar_wait(smem_u32(&s.bar_kv_full[g % NST]), (g / NST) & 1, p.err);
+        if (!__all_sync(0xffffffffu, wt)) { ok = false; break; }
+        tc_fence_after();  // after the softmax's tcgen05.ld of S
+        const uint64_t slot_off = static_cast<uint64_t>(((g % NST) * KVP * kKVBytes) >> 4);
+        if (leader) {
+          issue_qk<QP, KVP, kSAcc>(tmem + kTmemS, kv_a0 + slot_off, qk_b0, IDESC_QK);
+          mma_commit(smem_u32(&s.bar_s_full));
+        }
+        __syncwarp();
       }
-      __syncwarp();
+      gb += I.nblk;
     }
   } else if (warp == kPvWarp) {
     // =================================================================== PV issuer
-    // PV of block j once its P is written.  A warp of its own, so that PV is
-    // never queued behind the issue of the next block's QK.
+    // PV of block g once its P is written.  A warp of its own, so that PV is
+    // never queued behind the issue of the next QK.  An item's first PV
+    // overwrites O^T; its P is published only after the softmax warps have
+    // read the previous item's O^T.
     setmaxnreg_dec<kLowRegs>();
     const bool leader = elect_one();
     constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, kNH, 1, 1);
     const uint64_t pv_a0 = make_sdesc(smem_u32(s.kv[0][0]), kChunkBytes, 512, kSwizzle64B);
     const uint64_t plo0 = make_sdesc(smem_u32(s.plo), kChunkBytes, 512, kSwizzle64B);
-    for (int j = 0; j < nblk; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_p_full), j & 1, p.err))) break;
-      tc_fence_after();  // after the softmax's TMEM rescale of O^T
-      // O^T[512 vcols x 64 heads] += V^T P^T over the block's 128 keys, one
-      // 32-key quarter at a time with the four 128-column tiles interleaved;
-      // each quarter's rows go back to the gather when its MMAs complete.
-      // P hi sits in the slot's rope chunk, P lo in its own buffer.
-      const int slot = j % NST;
-      const uint64_t slot_off = static_cast<uint64_t>((slot * KVP * kKVBytes) >> 4);
-      if (leader) {
+    int gb = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
+      const Item I = item_at(p, w, groups);
+      for (int j = 0; j < I.nblk; ++j) {
+        const int g = gb + j;
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_p_full), g & 1, p.err))) { ok = false; break; }
+        tc_fence_after();  // after the softmax's TMEM reads and rescale of O^T
+        // O^T[512 vcols x 64 heads] += V^T P^T over the block's 128 keys, one
+        // 32-key quarter at a time with the four 128-column tiles interleaved;
+        // each quarter's rows go back to the gather when its MMAs complete.
+        // P hi sits in the slot's rope chunk, P lo in its own buffer.
+        const int slot = g % NST;
+        const uint64_t slot_off = static_cast<uint64_t>((slot * KVP * kKVBytes) >> 4);
+        if (leader) {
 #pragma unroll
-        for (int ks = 0; ks < kRowQ; ++ks) {
+          for (int ks = 0; ks < kRowQ; ++ks) {
 #pragma unroll
-          for (int pp = 0; pp < PP; ++pp)
+            for (int pp = 0; pp < PP; ++pp)
 #pragma unroll
-            for (int kp = 0; kp < KVP; ++kp)
+              for (int kp = 0; kp < KVP; ++kp)
 #pragma unroll
-              for (int tile = 0; tile < 4; ++tile) {
-                const uint32_t pacc = (j > 0 || pp > 0 || kp > 0 || ks > 0) ? 1u : 0u;
-                const uint64_t ad = pv_a0 + slot_off +
-                                    static_cast<uint64_t>((kp * kKVBytes + (2 * tile) * kChunkBytes + ks * 32 * 64) >> 4);
-                const uint64_t bd = pp == 0 ? pv_a0 + slot_off + static_cast<uint64_t>((kRope * kChunkBytes + ks * 32 * 64) >> 4)
-                                            : plo0 + static_cast<uint64_t>((ks * 32 * 64) >> 4);
-                mma_f8f6f4_ss(tmem + tile * kNH, ad, bd, IDESC_PV, pacc);
-              }
-          mma_commit(smem_u32(&s.bar_kv_empty[slot][ks]));
+                for (int tile = 0; tile < 4; ++tile) {
+                  const uint32_t pacc = (j > 0 || pp > 0 || kp > 0 || ks > 0) ? 1u : 0u;
+                  const uint64_t ad = pv_a0 + slot_off +
+                                      static_cast<uint64_t>((kp * kKVBytes + (2 * tile) * kChunkBytes + ks * 32 * 64) >> 4);
+                  const uint64_t bd = pp == 0 ? pv_a0 + slot_off + static_cast<uint64_t>((kRope * kChunkBytes + ks * 32 * 64) >> 4)
+                                              : plo0 + static_cast<uint64_t>((ks * 32 * 64) >> 4);
+                  mma_f8f6f4_ss(tmem + tile * kNH, ad, bd, IDESC_PV, pacc);
+                }
+            mma_commit(smem_u32(&s.bar_kv_empty[slot][ks]));
+          }
+          mma_commit(smem_u32(&s.bar_pv_done));
         }
-        mma_commit(smem_u32(&s.bar_pv_done));
+        __syncwarp();
       }
-      __syncwarp();
+      gb += I.nblk;
     }
   } else {
     // =================================================================== gather producers
     setmaxnreg_dec<kLowRegs>();
     const int pt = threadIdx.x - kProdWarp0 * 32;
-    const uint32_t first = tok_idx[0];
     const uint64_t keep = make_policy_evict_last();  // the latent pool stays in L2 over the q / out streams
     bool ok = true;
-    // Thread pt < 128 owns row pt of every block: its physical row and scale
-    // are loaded one block ahead.
-    uint32_t nxt_row = 0;
-    float nxt_sr = 1.f;
-    auto load_row = [&](int jb) {
-      const int key = jb * kBK + pt;
-      uint32_t row = key < n ? tok_idx[key] : first;
-      if (row >= static_cast<uint64_t>(p.phys_rows)) {
-        atomicOr(p.err, kErrIndex);
-        row = 0;
-      }
-      nxt_row = row;
-    };
-    auto load_scale = [&]() {
-      if (SC == kRow) {
-        nxt_sr = p.scales[static_cast<int64_t>(nxt_row) * p.nscale];
-      } else if (SC == kBlock) {
-        const float* sp = p.scales + static_cast<int64_t>(nxt_row) * p.nscale;
-        float sr = 0.f;
-        for (int b = 0; b < p.nscale; ++b) sr = fmaxf(sr, sp[b]);
-        nxt_sr = sr > 0.f ? sr : 1.f;
-      }
-    };
-    if (pt < kBK) {
-      load_row(0);
-      load_scale();
-    }
-    for (int j = 0; j < nblk; ++j) {
-      const int slot = j % NST;
-      const uint32_t par = ((j / NST) & 1) ^ 1;
-      const bool w = mbar_wait(smem_u32(&s.bar_kv_empty[slot][0]), par, p.err);
-      if (!named_bar_and(2, kProdThreads, ok && w)) break;
-      if (pt < kBK) {
-        s.idx[pt] = nxt_row;
-        s.srow[slot][pt] = nxt_sr;
-      }
-      named_bar_sync(2, kProdThreads);
-      // Key quarter q (rows 32q..32q+31) is refilled once PV of block j-NST
-      // has finished with it.
-      for (int q = 0; q < kRowQ; ++q) {
-        if (q > 0 && ok) ok = mbar_wait(smem_u32(&s.bar_kv_empty[slot][q]), par, p.err);
-        if (!ok) continue;
-        if (KVP == 1) {
-          // 32 rows x 36 16-byte pieces, consecutive threads on consecutive
-          // pieces of a row, into the SW64 operand layout
-#pragma unroll 4
-          for (int i = pt; i < 32 * 36; i += kProdThreads) {
-            const int row = 32 * q + i / 36, c = i % 36;
-            const int kc = c >> 2, c4 = c & 3;
-            const uint32_t dst = smem_u32(s.kv[slot][0]) + kc * kChunkBytes + row * 64 + sw64(row, c4);
-            cp_async16_hint(dst, p.latent + static_cast<int64_t>(s.idx[row]) * kD + c * 16, keep);
-          }
-        } else {
-          // blockwise rows: register dequantisation to x * s_blk / s_row, e4m3 hi + lo
-          for (int i = pt; i < 32 * 36; i += kProdThreads) {
-            const int row = 32 * q + i / 36, c = i % 36;
-            const int kc = c >> 2, c4 = c & 3;
-            const uint32_t rr = s.idx[row];
-            uint4 raw;
-            asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                         : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
-                         : "l"(p.latent + static_cast<int64_t>(rr) * kD + c * 16), "l"(keep));
-            const float ratio = p.scales[static_cast<int64_t>(rr) * p.nscale + (c >> 1)] / s.srow[slot][row];
-            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-            float x[16];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const float2 a = e4m3x2_to_f32x2(static_cast<uint16_t>(wv[k] & 0xffffu));
-              const float2 b = e4m3x2_to_f32x2(static_cast<uint16_t>(wv[k] >> 16));
-              x[4 * k + 0] = a.x * ratio;
-              x[4 * k + 1] = a.y * ratio;
-              x[4 * k + 2] = b.x * ratio;
-              x[4 * k + 3] = b.y * ratio;
-            }
-            uint4 hi, lo;
-            split16(x, hi, lo);
-            const uint32_t off = kc * kChunkBytes + row * 64 + sw64(row, c4);
-            *reinterpret_cast<uint4*>(&s.kv[slot][0][off]) = hi;
-            *reinterpret_cast<uint4*>(&s.kv[slot][KVP - 1][off]) = lo;
-          }
+    int gb = 0;
+    for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
+      const Item I = item_at(p, w, groups);
+      const int n = I.n;
+      if (n == 0) continue;
+      const uint32_t* tok_idx = p.indices + static_cast<int64_t>(I.t) * p.indices_stride;
+      const uint32_t first = tok_idx[0];
+      // Thread pt < 128 owns row pt of every block: its physical row and
+      // scale are loaded one block ahead.
+      uint32_t nxt_row = 0;
+      float nxt_sr = 1.f;
+      auto load_row = [&](int jb) {
+        const int key = jb * kBK + pt;
+        uint32_t row = key < n ? tok_idx[key] : first;
+        if (row >= static_cast<uint64_t>(p.phys_rows)) {
+          atomicOr(p.err, kErrIndex);
+          row = 0;
         }
-      }
-      // the next block's row and scale load while this block's rows land
-      if (pt < kBK && j + 1 < nblk) {
-        load_row(j + 1);
+        nxt_row = row;
+      };
+      auto load_scale = [&]() {
+        if (SC == kRow) {
+          nxt_sr = p.scales[static_cast<int64_t>(nxt_row) * p.nscale];
+        } else if (SC == kBlock) {
+          const float* sp = p.scales + static_cast<int64_t>(nxt_row) * p.nscale;
+          float sr = 0.f;
+          for (int b = 0; b < p.nscale; ++b) sr = fmaxf(sr, sp[b]);
+          nxt_sr = sr > 0.f ? sr : 1.f;
+        }
+      };
+      if (pt < kBK) {
+        load_row(0);
         load_scale();
       }
-      if (KVP == 1) cp_async_wait_all();
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&s.bar_kv_full[slot]));
+      for (int j = 0; j < I.nblk; ++j) {
+        const int g = gb + j;
+        const int slot = g % NST;
+        const uint32_t par = ((g / NST) & 1) ^ 1;
+        const bool wt = mbar_wait(smem_u32(&s.bar_kv_empty[slot][0]), par, p.err);
+        if (!named_bar_and(2, kProdThreads, ok && wt)) { ok = false; break; }
+        if (pt < kBK) {
+          s.idx[pt] = nxt_row;
+          s.srow[slot][pt] = nxt_sr;
+        }
+        named_bar_sync(2, kProdThreads);
+        // Key quarter q (rows 32q..32q+31) is refilled once PV of block g-NST
+        // has finished with it.
+        for (int q = 0; q < kRowQ; ++q) {
+          if (q > 0 && ok) ok = mbar_wait(smem_u32(&s.bar_kv_empty[slot][q]), par, p.err);
+          if (!ok) continue;
+          if (KVP == 1) {
+            // 32 rows x 36 16-byte pieces, consecutive threads on consecutive
+            // pieces of a row, into the SW64 operand layout
+#pragma unroll 2
+            for (int i = pt; i < 32 * 36; i += kProdThreads) {
+              const int row = 32 * q + i / 36, c = i % 36;
+              const uint32_t dst = smem_u32(s.kv[slot][0]) + (c >> 2) * kChunkBytes + row * 64 + sw64(row, c & 3);
+              cp_async16_hint(dst, p.latent + static_cast<int64_t>(s.idx[row]) * kD + c * 16, keep);
+            }
+          } else {
+            // blockwise rows: register dequantisation to x * s_blk / s_row, e4m3 hi + lo
+            for (int i = pt; i < 32 * 36; i += kProdThreads) {
+              const int row = 32 * q + i / 36, c = i % 36;
+              const int kc = c >> 2, c4 = c & 3;
+              const uint32_t rr = s.idx[row];
+              uint4 raw;
+              asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                           : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
+                           : "l"(p.latent + static_cast<int64_t>(rr) * kD + c * 16), "l"(keep));
+              const float ratio = p.scales[static_cast<int64_t>(rr) * p.nscale + (c >> 1)] / s.srow[slot][row];
+              const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+              float x[16];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float2 a = e4m3x2_to_f32x2(static_cast<uint16_t>(wv[k] & 0xffffu));
+                const float2 b = e4m3x2_to_f32x2(static_cast<uint16_t>(wv[k] >> 16));
+                x[4 * k + 0] = a.x * ratio;
+                x[4 * k + 1] = a.y * ratio;
+                x[4 * k + 2] = b.x * ratio;
+                x[4 * k + 3] = b.y * ratio;
+              }
+              uint4 hi, lo;
+              split16(x, hi, lo);
+              const uint32_t off = kc * kChunkBytes + row * 64 + sw64(row, c4);
+              *reinterpret_cast<uint4*>(&s.kv[slot][0][off]) = hi;
+              *reinterpret_cast<uint4*>(&s.kv[slot][KVP - 1][off]) = lo;
+            }
+          }
+        }
+        // the next block's row and scale load while this block's rows land
+        if (pt < kBK && j + 1 < I.nblk) {
+          load_row(j + 1);
+          load_scale();
+        }
+        if (KVP == 1) cp_async_wait_all();
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&s.bar_kv_full[slot]));
+      }
+      gb += I.nblk;
     }
   }
 
@@ -704,7 +808,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
 template <int QP, int KVP, int PP, int NST, int SC>
 static smla_status_t launch_t(const Params& p, cudaStream_t stream) {
   const size_t smem = sizeof(Smem<QP, KVP, PP, NST>);
-  if (smem > 232448) return fail(SMLA_ERR_UNSUPPORTED, "prefill variant needs %zu B of shared memory", smem);
+  static_assert(sizeof(Smem<QP, KVP, PP, NST>) <= 232448, "the variant's shared memory exceeds a CTA's 227 KB");
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<QP, KVP, PP, NST, SC>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return fail_cuda(e, "prefill smem attribute");
@@ -716,7 +820,9 @@ static smla_status_t launch_t(const Params& p, cudaStream_t stream) {
   if (fa.numRegs != kLaunchRegs)
     return fail(SMLA_ERR_UNSUPPORTED, "prefill kernel built with %d registers a thread, the register split needs %d",
                 fa.numRegs, kLaunchRegs);
-  dim3 grid(p.T, (p.H + kNH - 1) / kNH);
+  // persistent: one CTA per SM (shared memory allows no more), at most one per item
+  const int64_t items = static_cast<int64_t>(p.T) * ((p.H + kNH - 1) / kNH);
+  const dim3 grid(static_cast<unsigned>(std::min<int64_t>(items, device_sm_count())));
   prefill_kernel<QP, KVP, PP, NST, SC><<<grid, threads_for(KVP), smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, "prefill launch");

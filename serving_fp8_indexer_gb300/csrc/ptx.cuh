@@ -365,24 +365,12 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, int a_mn, in
          | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// ------------------------------------------------------------------ packed f32x2
-SMLA_DEVICE_INLINE uint64_t pack_f32x2(float lo, float hi) {
-  return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
-}
-SMLA_DEVICE_INLINE uint64_t pack_u32x2(uint32_t lo, uint32_t hi) {
-  return static_cast<uint64_t>(lo) | (static_cast<uint64_t>(hi) << 32);
-}
-SMLA_DEVICE_INLINE float2 unpack_f32x2(uint64_t v) {
-  return make_float2(__uint_as_float(static_cast<uint32_t>(v)), __uint_as_float(static_cast<uint32_t>(v >> 32)));
-}
-// a * b + c on both f32 halves (round to nearest)
-SMLA_DEVICE_INLINE uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-
 // ------------------------------------------------------------------ conversions
+// Two floats -> bf16x2 (round to nearest even), lo in the low half.
+SMLA_DEVICE_INLINE uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
 // Two floats -> two e4m3 bytes (round to nearest even, saturating), lo byte = a.
 SMLA_DEVICE_INLINE uint16_t f32x2_to_e4m3x2(float a, float b) {
   uint16_t r;
