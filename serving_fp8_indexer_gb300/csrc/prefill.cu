@@ -223,25 +223,6 @@ __device__ __forceinline__ Item item_at(const Params& p, int w, int groups) {
   return it;
 }
 
-// 8 x 8 transpose across the 8-lane groups of a warp: lane m of a group
-// holding e[i] = X[m][i] ends with e[i] = X[i][m].
-__device__ __forceinline__ void transpose8(float (&e)[8], int lane) {
-#pragma unroll
-  for (int sft = 1; sft < 8; sft <<= 1) {
-    const bool up = (lane & sft) != 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      if (i & sft) continue;
-      const float send = up ? e[i] : e[i | sft];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, sft);
-      if (up)
-        e[i] = recv;
-      else
-        e[i | sft] = recv;
-    }
-  }
-}
-
 // Persistent CTAs: CTA c takes the work items c, c + gridDim.x, ... in turn,
 // and every pipeline barrier keeps counting across items (a block's slot and
 // phases come from its index g over all of this CTA's blocks), so the next
@@ -311,63 +292,78 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     // softmax started only after its QK completed).
     auto load_q = [&](int w) {
       const Item I = item_at(p, w, groups);
-      const int hh = threadIdx.x >> 2, qtr = threadIdx.x & 3;
-      const bool hvalid = hh < I.hv;
-      const int64_t qrow = static_cast<int64_t>(I.t) * p.H + I.h0 + hh;
-      float sigma = 1.f;
+      const int64_t row0 = static_cast<int64_t>(I.t) * p.H + I.h0;  // the item's heads are contiguous in q
       if (QP == 2) {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + qrow * kD + qtr * 144);
-        uint4 v[18];
+        // 8 threads per head (two rounds of 32 heads): thread r8 of a head
+        // reads its 16-byte pieces r8, r8 + 8, ... (8 bf16 each), so a warp's
+        // load covers four heads' contiguous 128-byte runs; all 18 loads are
+        // in flight together.
+        const int r8 = threadIdx.x & 7;
+        uint4 v[2][9];
 #pragma unroll
-        for (int i = 0; i < 18; ++i) v[i] = hvalid ? ld_stream16(src + i) : make_uint4(0, 0, 0, 0);
-        float amax = 0.f;
+        for (int rd = 0; rd < 2; ++rd) {
+          const int hh = 32 * rd + (threadIdx.x >> 3);
+          const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + (row0 + hh) * kD);
 #pragma unroll
-        for (int i = 0; i < 18; ++i) {
-          const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            amax = fmaxf(amax, fabsf(__uint_as_float(wv[k] << 16)));
-            amax = fmaxf(amax, fabsf(__uint_as_float(wv[k] & 0xffff0000u)));
-          }
+          for (int k = 0; k < 9; ++k) v[rd][k] = hh < I.hv ? ld_stream16(src + r8 + 8 * k) : make_uint4(0, 0, 0, 0);
         }
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        int e = 0;
-        if (amax > 0.f) {
-          int ex;
-          frexpf(amax, &ex);  // amax = m * 2^ex, m in [0.5, 1)
-          e = 8 - ex;
-        }
-        sigma = ldexpf(1.f, e);
 #pragma unroll
-        for (int i = 0; i < 9; ++i) {
-          float x[16];
-          const uint32_t wv[8] = {v[2 * i].x, v[2 * i].y, v[2 * i].z, v[2 * i].w,
-                                  v[2 * i + 1].x, v[2 * i + 1].y, v[2 * i + 1].z, v[2 * i + 1].w};
+        for (int rd = 0; rd < 2; ++rd) {
+          const int hh = 32 * rd + (threadIdx.x >> 3);
+          float amax = 0.f;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            x[2 * k] = __uint_as_float(wv[k] << 16) * sigma;
-            x[2 * k + 1] = __uint_as_float(wv[k] & 0xffff0000u) * sigma;
+          for (int k = 0; k < 9; ++k) {
+            const uint32_t wv[4] = {v[rd][k].x, v[rd][k].y, v[rd][k].z, v[rd][k].w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              amax = fmaxf(amax, fabsf(__uint_as_float(wv[u] << 16)));
+              amax = fmaxf(amax, fabsf(__uint_as_float(wv[u] & 0xffff0000u)));
+            }
           }
-          uint4 hi, lo;
-          split16(x, hi, lo);
-          const int e0 = qtr * 144 + 16 * i;
-          const int kc = e0 >> 6, c4 = (e0 & 63) >> 4;
-          const uint32_t off = kc * (kQN * 64) + hh * 64 + sw64(hh, c4);
-          *reinterpret_cast<uint4*>(&s.q[off]) = hi;
-          *reinterpret_cast<uint4*>(&s.q[off + kNH * 64]) = lo;
+#pragma unroll
+          for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          // per-head power of two putting the largest |q| * 2^e in [128, 256)
+          int e = 0;
+          if (amax > 0.f) {
+            int ex;
+            frexpf(amax, &ex);  // amax = m * 2^ex, m in [0.5, 1)
+            e = 8 - ex;
+          }
+          const float sigma = ldexpf(1.f, e);
+#pragma unroll
+          for (int k = 0; k < 9; ++k) {
+            const uint32_t wv[4] = {v[rd][k].x, v[rd][k].y, v[rd][k].z, v[rd][k].w};
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              x[2 * u] = __uint_as_float(wv[u] << 16) * sigma;
+              x[2 * u + 1] = __uint_as_float(wv[u] & 0xffff0000u) * sigma;
+            }
+            uint2 hi, lo;
+            split8(x, hi, lo);
+            const int e0 = 8 * (r8 + 8 * k);  // first element of the piece
+            const int kc = e0 >> 6, c4 = (e0 & 63) >> 4;
+            const uint32_t off = kc * (kQN * 64) + hh * 64 + sw64(hh, c4) + (e0 & 8);
+            *reinterpret_cast<uint2*>(&s.q[off]) = hi;
+            *reinterpret_cast<uint2*>(&s.q[off + kNH * 64]) = lo;
+          }
+          if (r8 == 0) s.cs[hh] = p.softmax_scale * kLog2e / sigma;
         }
       } else {
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) + qrow * kD + qtr * 144);
+        // e4m3 q as is: 4 threads per head, pieces r4, r4 + 4, ... (16 values each)
+        const int hh = threadIdx.x >> 2, r4 = threadIdx.x & 3;
+        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) + (row0 + hh) * kD);
+        uint4 v[9];
 #pragma unroll
-        for (int i = 0; i < 9; ++i) {
-          const uint4 v = hvalid ? ld_stream16(src + i) : make_uint4(0, 0, 0, 0);
-          const int e0 = qtr * 144 + 16 * i;
+        for (int k = 0; k < 9; ++k) v[k] = hh < I.hv ? ld_stream16(src + r4 + 4 * k) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+          const int e0 = 16 * (r4 + 4 * k);
           const int kc = e0 >> 6, c4 = (e0 & 63) >> 4;
-          *reinterpret_cast<uint4*>(&s.q[kc * (kQN * 64) + hh * 64 + sw64(hh, c4)]) = v;
+          *reinterpret_cast<uint4*>(&s.q[kc * (kQN * 64) + hh * 64 + sw64(hh, c4)]) = v[k];
         }
+        if (r4 == 0) s.cs[hh] = p.softmax_scale * kLog2e;
       }
-      if (qtr == 0) s.cs[hh] = p.softmax_scale * kLog2e / sigma;
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&s.bar_q));
     };
@@ -582,29 +578,18 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
       named_bar_sync(1, kSoftThreads);
       if (done) {
         tc_fence_after();
-        // Each 8-lane group transposes 8 heads x 8 columns, so a lane writes
-        // 8 consecutive bf16 of one head (16 bytes) straight to `out`.
+        // thread = one value column: 32 consecutive columns of a head per warp store
 #pragma unroll 1
         for (int tile = 0; tile < 4; ++tile) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + tile * kNH + hb, v);
           tmem_wait_ld();
-          const int vcol0 = tile * 128 + (warp & 3) * 32 + 8 * (lane >> 3);
+          const int vcol = tile * 128 + r;
 #pragma unroll
-          for (int rd = 0; rd < 4; ++rd) {
-            float e[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) e[i] = __uint_as_float(v[8 * rd + i]);
-            transpose8(e, lane);
-            const int head = hb + 8 * rd + (lane & 7);
-            const float inv = linv[head];
-            uint4 o;
-            o.x = pack_bf16x2(e[0] * inv, e[1] * inv);
-            o.y = pack_bf16x2(e[2] * inv, e[3] * inv);
-            o.z = pack_bf16x2(e[4] * inv, e[5] * inv);
-            o.w = pack_bf16x2(e[6] * inv, e[7] * inv);
-            if (head < I.hv) __stcs(reinterpret_cast<uint4*>(out_t + static_cast<int64_t>(head) * kDV + vcol0), o);
-          }
+          for (int h = 0; h < 32; ++h)
+            if (hb + h < I.hv)
+              __stcs(out_t + static_cast<int64_t>(hb + h) * kDV + vcol,
+                     __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[h]) * linv[hb + h])));
         }
       }
       // linv (s.fac) is rewritten by the next item's slow path only after the

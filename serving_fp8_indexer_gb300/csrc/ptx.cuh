@@ -366,11 +366,6 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, int a_mn, in
 }
 
 // ------------------------------------------------------------------ conversions
-// Two floats -> bf16x2 (round to nearest even), lo in the low half.
-SMLA_DEVICE_INLINE uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
 // Two floats -> two e4m3 bytes (round to nearest even, saturating), lo byte = a.
 SMLA_DEVICE_INLINE uint16_t f32x2_to_e4m3x2(float a, float b) {
   uint16_t r;
