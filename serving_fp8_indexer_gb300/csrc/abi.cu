@@ -36,12 +36,17 @@ smla_status_t fail_cuda(cudaError_t e, const char* what) {
   return fail(SMLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-bool encode_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
-                      uint32_t box_rows, int swizzle_bytes) {
-  const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {inner};
-  const cuuint32_t box[2] = {box_inner, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
+bool encode_tma_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                   const uint32_t* box, int swizzle_bytes) {
+  if (rank < 1 || rank > 5) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], estr[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    estr[i] = 1;
+    if (i + 1 < rank) st[i] = strides[i];
+  }
   // The driver entry point is looked up through the runtime, so the library
   // does not link libcuda directly (it loads on machines without a driver).
   using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -60,11 +65,19 @@ bool encode_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64
       encode = reinterpret_cast<EncodeFn>(fn);
     }
   }
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE,
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, static_cast<cuuint32_t>(rank), const_cast<void*>(base),
+                            d, st, bx, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                             swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool encode_tma_2d_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                      uint32_t box_rows, int swizzle_bytes) {
+  const uint64_t dims[2] = {inner, rows};
+  const uint64_t strides[1] = {inner};
+  const uint32_t box[2] = {box_inner, box_rows};
+  return encode_tma_u8(map, base, 2, dims, strides, box, swizzle_bytes);
 }
 
 static smla_status_t device_err_ptr(unsigned** out) {

@@ -110,6 +110,7 @@ struct Params {
   float softmax_scale;
   uint16_t* out;
   unsigned* err;
+  int q_box3d;  // q tensor map is 3-D: one load brings all column boxes of an item
 };
 
 template <int QP, int KVP, int PP, int NST>
@@ -126,9 +127,10 @@ struct Smem {
   float delta[kNH];      // reference raise of the current block
   float fac[kNH];        // rescale factor of the current block; 1 / row sum at the end
   int mx[kNH];           // block maximum per head (order-preserving ints)
-  unsigned long long bar_q, bar_kv_full[NST], bar_kv_empty[NST][kRowQ];
+  unsigned long long bar_qraw, bar_q, bar_kv_full[NST], bar_kv_empty[NST][kRowQ];
   unsigned long long bar_s_full, bar_s_free, bar_p_full, bar_pv_done;
   uint32_t tmem_base;
+  int q_issued;  // TMA q loads requested by the QK warp (read at exit)
 };
 
 __device__ __forceinline__ int ord_int(float f) {
@@ -208,12 +210,13 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t a0, uint64_t 
 struct Item {
   int t, h0, hv, n, nblk;
 };
-__device__ __forceinline__ Item item_at(const Params& p, int w, int groups) {
+// item w from its token's selection length
+__device__ __forceinline__ Item item_make(const Params& p, int w, int groups, uint32_t len) {
   Item it;
   it.t = w / groups;
   it.h0 = (w % groups) * kNH;
   it.hv = min(kNH, p.H - it.h0);
-  int n = static_cast<int>(p.lens[it.t]);
+  int n = static_cast<int>(len);
   if (n > p.indices_stride) {
     if (threadIdx.x == 0) atomicOr(p.err, kErrShape);
     n = p.indices_stride;
@@ -221,6 +224,9 @@ __device__ __forceinline__ Item item_at(const Params& p, int w, int groups) {
   it.n = n;
   it.nblk = (n + kBK - 1) / kBK;
   return it;
+}
+__device__ __forceinline__ Item item_at(const Params& p, int w, int groups) {
+  return item_make(p, w, groups, p.lens[w / groups]);
 }
 
 // Persistent CTAs: CTA c takes the work items c, c + gridDim.x, ... in turn,
@@ -230,7 +236,7 @@ __device__ __forceinline__ Item item_at(const Params& p, int w, int groups) {
 // last blocks and epilogue run.
 template <int QP, int KVP, int PP, int NST, int SC>
 __global__ void __launch_bounds__(threads_for(KVP), 1)
-    prefill_kernel(const Params p) {
+    prefill_kernel(const __grid_constant__ CUtensorMap tq, const Params p) {
   using S = Smem<QP, KVP, PP, NST>;
   static_assert(!(PP == 2 && KVP == 2), "P lo has a buffer only when rows are single-term");
   // S^T accumulators: the block's QK MMAs alternate between two of them
@@ -256,6 +262,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
   const int items = p.T * groups;
 
   if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&s.bar_qraw), 1);
     mbar_init(smem_u32(&s.bar_q), kSoftThreads);
     for (int i = 0; i < NST; ++i) {
       mbar_init(smem_u32(&s.bar_kv_full[i]), kProdThreads);
@@ -266,6 +273,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     mbar_init(smem_u32(&s.bar_p_full), kSoftThreads);
     mbar_init(smem_u32(&s.bar_pv_done), 1);
     fence_mbar_init();
+    tma_prefetch_desc(&tq);
   }
   if (threadIdx.x < kNH) s.mx[threadIdx.x] = kOrdMin;
   if (warp == kMmaWarp) {
@@ -276,6 +284,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
+  int q_waited = 0;  // TMA q loads waited by the softmax warps (bar_qraw phases)
 
   if (warp < kSoftWarps) {
     // =================================================================== softmax / epilogue
@@ -284,28 +293,34 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     const int half = warp >> 2;             // heads [32*half, 32*half + 32)
     const int hb = half * 32;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    // ---- q of item w into s.q (its QK B operand) and its scales into s.cs:
-    // 4 threads per head, 144 elements each, all loads in flight at once;
-    // bf16 q is split into e4m3 hi + lo with a per-head power of two that
-    // puts the largest |q| * 2^e in [128, 256).  Called once s.q is free
-    // (before the first item, then after an item's last block, whose
-    // softmax started only after its QK completed).
-    auto load_q = [&](int w) {
-      const Item I = item_at(p, w, groups);
-      const int64_t row0 = static_cast<int64_t>(I.t) * p.H + I.h0;  // the item's heads are contiguous in q
+    // ---- q of an item into s.q (its QK B operand).  The QK warp requests
+    // the item's 64 q rows with TMA (see there) in the SW64 layout, head =
+    // row, 64-byte column box c at c * 4096.  e4m3 q lands in its final
+    // layout.  For bf16 q, box pair (2kc, 2kc+1) covers exactly the bytes of
+    // chunk kc's hi and lo rows, so the split into e4m3 hi + lo (per-head
+    // power of two putting the largest |q| * 2^e in [128, 256)) runs in
+    // place, each head's bytes read and rewritten by the same eight lanes.
+    auto wait_q = [&]() -> bool {
+      const bool r = named_bar_and(1, kSoftThreads, mbar_wait(smem_u32(&s.bar_qraw), q_waited & 1, p.err));
+      ++q_waited;
+      return r;
+    };
+    // waits for item I's q rows, splits bf16 q, sets s.cs and releases s.q to QK
+    auto convert_q = [&](const Item& I) -> bool {
+      if (!wait_q()) return false;
       if (QP == 2) {
-        // 8 threads per head (two rounds of 32 heads): thread r8 of a head
-        // reads its 16-byte pieces r8, r8 + 8, ... (8 bf16 each), so a warp's
-        // load covers four heads' contiguous 128-byte runs; all 18 loads are
-        // in flight together.
+        // 8 lanes per head (two rounds of 32 heads): lane r8 of a head holds
+        // elements 8 * (r8 + 8k) .. +7 of the row (box 2k + r8 / 4, piece r8 % 4)
         const int r8 = threadIdx.x & 7;
         uint4 v[2][9];
 #pragma unroll
         for (int rd = 0; rd < 2; ++rd) {
           const int hh = 32 * rd + (threadIdx.x >> 3);
-          const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + (row0 + hh) * kD);
 #pragma unroll
-          for (int k = 0; k < 9; ++k) v[rd][k] = hh < I.hv ? ld_stream16(src + r8 + 8 * k) : make_uint4(0, 0, 0, 0);
+          for (int k = 0; k < 9; ++k)
+            v[rd][k] = hh < I.hv ? *reinterpret_cast<const uint4*>(&s.q[(2 * k + (r8 >> 2)) * (kNH * 64) + hh * 64 +
+                                                                         sw64(hh, r8 & 3)])
+                                 : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int rd = 0; rd < 2; ++rd) {
@@ -322,7 +337,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
           }
 #pragma unroll
           for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-          // per-head power of two putting the largest |q| * 2^e in [128, 256)
+          __syncwarp();  // the head's eight lanes have read all of its bytes
           int e = 0;
           if (amax > 0.f) {
             int ex;
@@ -350,45 +365,36 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
           if (r8 == 0) s.cs[hh] = p.softmax_scale * kLog2e / sigma;
         }
       } else {
-        // e4m3 q as is: 4 threads per head, pieces r4, r4 + 4, ... (16 values each)
-        const int hh = threadIdx.x >> 2, r4 = threadIdx.x & 3;
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) + (row0 + hh) * kD);
-        uint4 v[9];
-#pragma unroll
-        for (int k = 0; k < 9; ++k) v[k] = hh < I.hv ? ld_stream16(src + r4 + 4 * k) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int k = 0; k < 9; ++k) {
-          const int e0 = 16 * (r4 + 4 * k);
-          const int kc = e0 >> 6, c4 = (e0 & 63) >> 4;
-          *reinterpret_cast<uint4*>(&s.q[kc * (kQN * 64) + hh * 64 + sw64(hh, c4)]) = v[k];
-        }
-        if (r4 == 0) s.cs[hh] = p.softmax_scale * kLog2e;
+        // e4m3 q is in place; rows past the item's heads (another token's) are zeroed
+        if (I.hv < kNH)
+          for (int i = threadIdx.x; i < kChunks * kNH * 4; i += kSoftThreads) {
+            const int row = (i >> 2) % kNH;
+            if (row >= I.hv) *reinterpret_cast<uint4*>(&s.q[(i >> 2) * 64 + (i & 3) * 16]) = make_uint4(0, 0, 0, 0);
+          }
+        if (threadIdx.x < kNH) s.cs[threadIdx.x] = p.softmax_scale * kLog2e;
       }
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&s.bar_q));
-    };
-    // the next item after w that has keys (items past the end: none)
-    auto next_nonempty = [&](int w) {
-      for (w += gridDim.x; w < items; w += gridDim.x)
-        if (item_at(p, w, groups).n > 0) return w;
-      return items;
+      return true;
     };
     int gb = 0;  // index of the item's first block among this CTA's blocks
     bool ok = true;
-    {
-      const int w0 = blockIdx.x < items && item_at(p, blockIdx.x, groups).n > 0 ? static_cast<int>(blockIdx.x)
-                                                                                  : next_nonempty(blockIdx.x);
-      if (w0 < items) load_q(w0);
-    }
+    bool q_in = false;  // s.q holds the current item's converted q
+    Item I = item_at(p, blockIdx.x, groups);
     for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
-      const Item I = item_at(p, w, groups);
+      const int wn = w + static_cast<int>(gridDim.x);  // this CTA's next item
       const int n = I.n, nblk = I.nblk;
       uint16_t* out_t = p.out + (static_cast<int64_t>(I.t) * p.H + I.h0) * kDV;
-      if (n == 0) {  // empty selection: zeros (no softmax mass)
+      if (n == 0) {  // empty selection: zeros (no softmax mass); the QK warp skips it
         for (int i = threadIdx.x; i < I.hv * kDV / 8; i += kSoftThreads)
           __stcs(reinterpret_cast<uint4*>(out_t) + i, make_uint4(0, 0, 0, 0));
+        if (wn < items) I = item_at(p, wn, groups);
         continue;
       }
+      if (!q_in && !convert_q(I)) { ok = false; break; }  // first item, or after an empty one
+      q_in = false;
+      // selection length of item wn: loaded now, used by the epilogue
+      const uint32_t len_next = wn < items ? p.lens[wn / groups] : 0u;
       if (threadIdx.x < kNH) s.negm[threadIdx.x] = 0.f;  // block 0 sets the reference
       named_bar_sync(1, kSoftThreads);
       // lv[h]: this key lane's share of head hb+h's softmax denominator,
@@ -563,11 +569,15 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         }
         atomicAdd(&linv[hb + lane], lv[0]);
       }
-      // the next item's q while this item's last PV runs (its QK is done),
-      // so the next QK overlaps this epilogue
-      {
-        const int wn = next_nonempty(w);
-        if (wn < items) load_q(wn);
+      // the next item's q while this item's last PV runs, so the next QK
+      // overlaps this epilogue
+      Item In{};
+      if (wn < items) {
+        In = item_make(p, wn, groups, len_next);
+        if (In.n > 0) {
+          if (!convert_q(In)) { ok = false; break; }
+          q_in = true;
+        }
       }
       // ---- O^T / l -> bf16 once the last PV has completed
       const bool done = named_bar_and(1, kSoftThreads, mbar_wait(smem_u32(&s.bar_pv_done), (gb - 1) & 1, p.err));
@@ -594,6 +604,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
       }
       // linv (s.fac) is rewritten by the next item's slow path only after the
       // named barrier at that item's start; every thread has read it by then
+      I = In;
     }
   } else if (warp == kMmaWarp) {
     // =================================================================== QK issuer
@@ -605,8 +616,38 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     constexpr uint32_t IDESC_QK = idesc_e4m3_f32(kBK, kQN, 0, 0);
     const uint64_t qk_b0 = make_sdesc(smem_u32(s.q), 16, 512, kSwizzle64B);
     const uint64_t kv_a0 = make_sdesc(smem_u32(s.kv[0][0]), 16, 512, kSwizzle64B);
+    // q of the CTA's next item with keys, requested once the last QK of the
+    // item before it has completed (s.q is then free).  With a 3-D tensor
+    // map one load brings all column boxes, else one load per box.
+    constexpr int kQBoxes = QP == 2 ? 2 * kChunks : kChunks;
+    const uint64_t q_policy = make_policy_evict_first();  // q is read once
+    int q_issued = 0;
+    auto issue_q = [&](int w) {
+      ++q_issued;
+      if (leader) {
+        const int row = w / groups * p.H + (w % groups) * kNH;
+        mbar_arrive_expect_tx(smem_u32(&s.bar_qraw), kQBoxes * kNH * 64);
+        if (p.q_box3d) {
+          tma_load_3d_hint(smem_u32(s.q), &tq, 0, row, 0, smem_u32(&s.bar_qraw), q_policy);
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < kQBoxes; ++c)
+            tma_load_2d_hint(smem_u32(s.q) + c * (kNH * 64), &tq, 64 * c, row, smem_u32(&s.bar_qraw), q_policy);
+        }
+      }
+      __syncwarp();
+    };
+    auto next_nonempty = [&](int w) {
+      for (w += gridDim.x; w < items; w += gridDim.x)
+        if (item_at(p, w, groups).n > 0) return w;
+      return items;
+    };
     int qn = 0, gb = 0;
     bool ok = true;
+    {
+      const int w0 = item_at(p, blockIdx.x, groups).n > 0 ? static_cast<int>(blockIdx.x) : next_nonempty(blockIdx.x);
+      if (w0 < items) issue_q(w0);
+    }
     for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
       const Item I = item_at(p, w, groups);
       if (I.n == 0) continue;
@@ -626,7 +667,15 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         __syncwarp();
       }
       gb += I.nblk;
+      if (!ok) break;
+      const int wn = next_nonempty(w);
+      if (wn < items) {
+        // s.q is overwritten only after this item's last QK has completed
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_s_full), (gb - 1) & 1, p.err));
+        if (ok) issue_q(wn);
+      }
     }
+    if (leader) s.q_issued = q_issued;
   } else if (warp == kPvWarp) {
     // =================================================================== PV issuer
     // PV of block g once its P is written.  A warp of its own, so that PV is
@@ -787,11 +836,13 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // a q load still in flight after an error is waited for (bounded) before exit
+  if (threadIdx.x == 0 && s.q_issued > q_waited) mbar_wait(smem_u32(&s.bar_qraw), q_waited & 1, p.err);
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int QP, int KVP, int PP, int NST, int SC>
-static smla_status_t launch_t(const Params& p, cudaStream_t stream) {
+static smla_status_t launch_t(const CUtensorMap& tq, const Params& p, cudaStream_t stream) {
   const size_t smem = sizeof(Smem<QP, KVP, PP, NST>);
   static_assert(sizeof(Smem<QP, KVP, PP, NST>) <= 232448, "the variant's shared memory exceeds a CTA's 227 KB");
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<QP, KVP, PP, NST, SC>,
@@ -808,7 +859,7 @@ static smla_status_t launch_t(const Params& p, cudaStream_t stream) {
   // persistent: one CTA per SM (shared memory allows no more), at most one per item
   const int64_t items = static_cast<int64_t>(p.T) * ((p.H + kNH - 1) / kNH);
   const dim3 grid(static_cast<unsigned>(std::min<int64_t>(items, device_sm_count())));
-  prefill_kernel<QP, KVP, PP, NST, SC><<<grid, threads_for(KVP), smem, stream>>>(p);
+  prefill_kernel<QP, KVP, PP, NST, SC><<<grid, threads_for(KVP), smem, stream>>>(tq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, "prefill launch");
   return SMLA_OK;
@@ -822,12 +873,26 @@ smla_status_t launch_sparse_prefill(const void* q, int q_dtype, const uint8_t* l
                                     unsigned* err, cudaStream_t stream) {
   using namespace pf;
   const int nscale = sbs == 0 ? 0 : (kD + sbs - 1) / sbs;
-  Params p{q, latent, phys_rows, scales, nscale, indices, indices_stride, topk_lengths, T, H, softmax_scale, out, err};
+  Params p{q, latent, phys_rows, scales, nscale, indices, indices_stride, topk_lengths, T, H, softmax_scale, out, err, 0};
   const bool bf16 = q_dtype == SMLA_BF16;
-  if (sbs == 0) return bf16 ? launch_t<2, 1, 2, 2, kUnit>(p, stream) : launch_t<1, 1, 1, 2, kUnit>(p, stream);
-  if (sbs >= kD) return bf16 ? launch_t<2, 1, 2, 2, kRow>(p, stream) : launch_t<1, 1, 1, 2, kRow>(p, stream);
-  if (bf16) return fail(SMLA_ERR_UNSUPPORTED, "bf16 q with block scales is not built (shared memory)");
-  return launch_t<1, 2, 1, 1, kBlock>(p, stream);
+  if (bf16 && sbs != 0 && sbs < kD) return fail(SMLA_ERR_UNSUPPORTED, "bf16 q with block scales is not built (shared memory)");
+  // q rows [T * H] x (576 elements) as bytes, loaded as 64-byte column boxes
+  // of 64 rows: preferably one 3-D box (x = byte in the box, y = row, z =
+  // box index with a 64-byte stride), else a 2-D map with one load per box.
+  CUtensorMap tq;
+  const uint64_t pitch = static_cast<uint64_t>(kD) * (bf16 ? 2 : 1);
+  const uint32_t nbox = static_cast<uint32_t>(pitch / 64);
+  {
+    const uint64_t dims[3] = {64, static_cast<uint64_t>(T) * H, nbox};
+    const uint64_t strides[2] = {pitch, 64};
+    const uint32_t box[3] = {64, static_cast<uint32_t>(kNH), nbox};
+    p.q_box3d = encode_tma_u8(&tq, q, 3, dims, strides, box, 64) ? 1 : 0;
+  }
+  if (!p.q_box3d && !encode_tma_2d_u8(&tq, q, pitch, static_cast<uint64_t>(T) * H, 64, kNH, 64))
+    return fail(SMLA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the prefill q tensor map");
+  if (sbs == 0) return bf16 ? launch_t<2, 1, 2, 2, kUnit>(tq, p, stream) : launch_t<1, 1, 1, 2, kUnit>(tq, p, stream);
+  if (sbs >= kD) return bf16 ? launch_t<2, 1, 2, 2, kRow>(tq, p, stream) : launch_t<1, 1, 1, 2, kRow>(tq, p, stream);
+  return launch_t<1, 2, 1, 1, kBlock>(tq, p, stream);
 }
 
 }  // namespace smla

@@ -6,7 +6,7 @@ import torch
 
 from serving_fp8_indexer_gb300 import workloads as wl
 
-from _gpu_helpers import (check_prefill, rows_of, run_indexer, run_prefill, run_topk, sample_tokens)
+from _gpu_helpers import (check_prefill, q_attn_tensor, rows_of, run_indexer, run_prefill, run_topk, sample_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -114,3 +114,19 @@ def test_blockwise_fp8_full_size_sampled():
 def test_e2e_chunk_full_size_sampled():
     w = wl.e2e_chunk()
     _end_to_end(w, sample_tokens(w.seqs, 3))
+
+
+def test_prefill_repeats_are_stable():
+    # Several items per CTA with one- and two-block selections: a pipeline
+    # race shows up as a run that differs from the first.  The row-sum
+    # atomics may add in another order (a few bf16 ulps).
+    w = wl.dsv32_prefill(T=300, k=256)
+    idx = torch.from_numpy(w.indices).cuda()
+    lens = torch.from_numpy(w.topk_lengths).cuda()
+    q = q_attn_tensor(w)
+    first = run_prefill(w, idx, lens, q=q).float()
+    assert torch.isfinite(first).all()
+    for _ in range(100):
+        out = run_prefill(w, idx, lens, q=q).float()
+        assert torch.isfinite(out).all()
+        assert float((out - first).abs().max()) <= 1e-2
