@@ -588,18 +588,25 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
       named_bar_sync(1, kSoftThreads);
       if (done) {
         tc_fence_after();
-        // thread = one value column: 32 consecutive columns of a head per warp store
+        // thread = one value column.  Lane pairs swap one value per two heads,
+        // so the even lane holds columns (c, c+1) of head h and the odd lane
+        // those of head h+1: one 4-byte bf16x2 store each.
+        const bool odd = (lane & 1) != 0;
 #pragma unroll 1
         for (int tile = 0; tile < 4; ++tile) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_base + tile * kNH + hb, v);
           tmem_wait_ld();
-          const int vcol = tile * 128 + r;
+          uint32_t* o2 = reinterpret_cast<uint32_t*>(out_t + tile * 128 + (r & ~1));
 #pragma unroll
-          for (int h = 0; h < 32; ++h)
-            if (hb + h < I.hv)
-              __stcs(out_t + static_cast<int64_t>(hb + h) * kDV + vcol,
-                     __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[h]) * linv[hb + h])));
+          for (int h = 0; h < 32; h += 2) {
+            const float a = __uint_as_float(v[h]) * linv[hb + h];
+            const float b = __uint_as_float(v[h + 1]) * linv[hb + h + 1];
+            const float got = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+            const __nv_bfloat162 pr = odd ? __floats2bfloat162_rn(got, b) : __floats2bfloat162_rn(a, got);
+            const int head = hb + h + (odd ? 1 : 0);
+            if (head < I.hv) __stcs(o2 + static_cast<int64_t>(head) * (kDV / 2), *reinterpret_cast<const uint32_t*>(&pr));
+          }
         }
       }
       // linv (s.fac) is rewritten by the next item's slow path only after the
