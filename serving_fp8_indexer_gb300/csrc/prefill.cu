@@ -54,6 +54,7 @@
 // owner, warp 9 PV issuer, warps 10-23 gather producers (cp.async 16 B into
 // the SW64 layout, or a register dequantisation of blockwise rows).
 #include <algorithm>
+#include <cstddef>
 
 #include "ptx.cuh"
 #include "smla_internal.h"
@@ -71,6 +72,7 @@ constexpr int kKVBytes = kChunks * kBK * 64;  // 73728
 constexpr int kChunkBytes = kBK * 64;         // 8192: one 64-column chunk of a block
 constexpr int kRope = 8;                      // chunk index of columns 512..575
 constexpr int kRowQ = 4;                      // key quarters a slot is released in
+constexpr int kBlkScales = kD / 32;           // 32-column block scales per row (blockwise rows)
 constexpr int kSoftWarps = 8;
 constexpr int kSoftThreads = kSoftWarps * 32;
 constexpr int kMmaWarp = 8;   // QK issuer, TMEM owner
@@ -122,13 +124,16 @@ struct Smem {
   uint8_t plo[PP == 2 ? kChunkBytes : 16];  // P lo term (bf16 path)
   uint32_t idx[kBK];
   float srow[NST][kBK];  // per-row scale (1 for unit)
-  float cs[kNH];         // softmax_scale * log2(e) / 2^e_h
-  float negm[kNH];       // minus the reference maximum per head (log2 units)
+  // blockwise rows: each row's 18 block scales, then 1 / s_row per row
+  float bsc[KVP == 2 ? kBK * kBlkScales + kBK : 4];
+  alignas(16) float cs[kNH];    // softmax_scale * log2(e) / 2^e_h (read as float4)
+  alignas(16) float negm[kNH];  // minus the reference maximum per head, log2 units (read as float4)
   float delta[kNH];      // reference raise of the current block
   float fac[kNH];        // rescale factor of the current block; 1 / row sum at the end
   int mx[kNH];           // block maximum per head (order-preserving ints)
   unsigned long long bar_qraw, bar_q, bar_kv_full[NST], bar_kv_empty[NST][kRowQ];
   unsigned long long bar_s_full, bar_s_free, bar_p_full, bar_pv_done;
+  unsigned long long bar_kv_split;  // blockwise rows: the block's hi / lo terms are written
   uint32_t tmem_base;
   int q_issued;  // TMA q loads requested by the QK warp (read at exit)
 };
@@ -182,6 +187,39 @@ __device__ __forceinline__ uint4 quant16(const float (&x)[16]) {
     w[i] = static_cast<uint32_t>(f32x2_to_e4m3x2(x[4 * i], x[4 * i + 1])) |
            (static_cast<uint32_t>(f32x2_to_e4m3x2(x[4 * i + 2], x[4 * i + 3])) << 16);
   return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Blockwise rows: the softmax warps split a landed block in place.  A piece
+// is 16 bytes (16 e4m3 values) of one row; a warp covers 8 rows x 4 pieces of
+// one 64-byte chunk (512 contiguous bytes: no bank conflicts).  x = e4m3 *
+// (s_blk / s_row) in f16 (the product needs 8 significant bits, f16 keeps
+// 11), hi = x rounded to e4m3's 3 mantissa bits (nearest even, on the f16
+// bits), lo = x - hi (exact); hi overwrites the raw piece, lo goes to the
+// second buffer.  bsc holds 18 block scales per row, then 1 / s_row per row.
+__device__ __forceinline__ void split_block(uint8_t* hi_buf, uint8_t* lo_buf, const float* bsc) {
+  for (int i = threadIdx.x; i < kBK * 36; i += kSoftThreads) {
+    const int kc = i >> 9, row = (i >> 2) & (kBK - 1), c4 = i & 3;
+    const uint32_t off = kc * kChunkBytes + row * 64 + sw64(row, c4);
+    const uint4 raw = *reinterpret_cast<const uint4*>(hi_buf + off);
+    const float ratio = bsc[row * kBlkScales + 2 * kc + (c4 >> 1)] * bsc[kBK * kBlkScales + row];
+    const uint32_t r2 = f32x2_to_f16x2(ratio, ratio);
+    const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t xh[2], hh[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        xh[u] = hmul2(e4m3x2_to_f16x2(static_cast<uint16_t>(u == 0 ? wv[k] & 0xffffu : wv[k] >> 16)), r2);
+        hh[u] = (xh[u] + 0x003f003fu + ((xh[u] >> 7) & 0x00010001u)) & 0xff80ff80u;
+      }
+      h[k] = static_cast<uint32_t>(f16x2_to_e4m3x2(hh[0])) | (static_cast<uint32_t>(f16x2_to_e4m3x2(hh[1])) << 16);
+      l[k] = static_cast<uint32_t>(f16x2_to_e4m3x2(hsub2(xh[0], hh[0]))) |
+             (static_cast<uint32_t>(f16x2_to_e4m3x2(hsub2(xh[1], hh[1]))) << 16);
+    }
+    *reinterpret_cast<uint4*>(hi_buf + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo_buf + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
 }
 
 // Issues QK of one block: S^T[128 keys x QP*64] over the 576 columns (for
@@ -239,6 +277,9 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const Params p) {
   using S = Smem<QP, KVP, PP, NST>;
   static_assert(!(PP == 2 && KVP == 2), "P lo has a buffer only when rows are single-term");
+  static_assert(offsetof(S, kv) % 1024 == 0 && offsetof(S, plo) % 1024 == 0,
+                "swizzled operand tiles need 1024-byte alignment");
+  static_assert(offsetof(S, cs) % 16 == 0 && offsetof(S, negm) % 16 == 0, "cs / negm are read as float4");
   // S^T accumulators: the block's QK MMAs alternate between two of them
   // (summed by the softmax), because an MMA waits for the previous one on
   // its accumulator but not for other MMAs (measured: two alternating
@@ -272,6 +313,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     mbar_init(smem_u32(&s.bar_s_free), kSoftThreads);
     mbar_init(smem_u32(&s.bar_p_full), kSoftThreads);
     mbar_init(smem_u32(&s.bar_pv_done), 1);
+    mbar_init(smem_u32(&s.bar_kv_split), kSoftThreads);
     fence_mbar_init();
     tma_prefetch_desc(&tq);
   }
@@ -408,8 +450,26 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         const int slot = g % NST;
         // S^T of block j is ready; kv_full is also waited so that the
         // producers' per-row scales are visible to this thread.
-        bool wt = mbar_wait(smem_u32(&s.bar_s_full), g & 1, p.err) &&
-                  mbar_wait(smem_u32(&s.bar_kv_full[slot]), (g / NST) & 1, p.err);
+        bool wt = mbar_wait(smem_u32(&s.bar_kv_full[slot]), (g / NST) & 1, p.err);
+        if (KVP == 2) {
+          // Blockwise rows landed raw: s_row = the row's largest block scale
+          // (1 if none is positive), then in place x * s_blk / s_row -> e4m3
+          // hi (over the raw piece) + lo, released to QK by kv_split.
+          if (!named_bar_and(1, kSoftThreads, wt)) { ok = false; break; }
+          if (threadIdx.x < kBK) {
+            float sr = 0.f;
+#pragma unroll
+            for (int b = 0; b < kBlkScales; ++b) sr = fmaxf(sr, s.bsc[threadIdx.x * kBlkScales + b]);
+            sr = sr > 0.f ? sr : 1.f;
+            s.srow[slot][threadIdx.x] = sr;
+            s.bsc[kBK * kBlkScales + threadIdx.x] = 1.f / sr;
+          }
+          named_bar_sync(1, kSoftThreads);
+          split_block(s.kv[slot][0], s.kv[slot][KVP - 1], s.bsc);
+          fence_proxy_async_smem();
+          mbar_arrive(smem_u32(&s.bar_kv_split));
+        }
+        wt = wt && mbar_wait(smem_u32(&s.bar_s_full), g & 1, p.err);
         if (!named_bar_and(1, kSoftThreads, wt)) { ok = false; break; }
         tc_fence_after();
         float y[32];
@@ -663,7 +723,8 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
       for (int j = 0; ok && j < I.nblk; ++j) {
         const int g = gb + j;
         const bool wt = (g == 0 || mbar_wait(smem_u32(&s.bar_s_free), (g - 1) & 1, p.err)) &&
-                        mbar_wait(smem_u32(&s.bar_kv_full[g % NST]), (g / NST) & 1, p.err);
+                        (KVP == 2 ? mbar_wait(smem_u32(&s.bar_kv_split), g & 1, p.err)
+                                  : mbar_wait(smem_u32(&s.bar_kv_full[g % NST]), (g / NST) & 1, p.err));
         if (!__all_sync(0xffffffffu, wt)) { ok = false; break; }
         tc_fence_after();  // after the softmax's tcgen05.ld of S
         const uint64_t slot_off = static_cast<uint64_t>(((g % NST) * KVP * kKVBytes) >> 4);
@@ -758,15 +819,8 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         }
         nxt_row = row;
       };
-      auto load_scale = [&]() {
-        if (SC == kRow) {
-          nxt_sr = p.scales[static_cast<int64_t>(nxt_row) * p.nscale];
-        } else if (SC == kBlock) {
-          const float* sp = p.scales + static_cast<int64_t>(nxt_row) * p.nscale;
-          float sr = 0.f;
-          for (int b = 0; b < p.nscale; ++b) sr = fmaxf(sr, sp[b]);
-          nxt_sr = sr > 0.f ? sr : 1.f;
-        }
+      auto load_scale = [&]() {  // block scales are gathered with the rows
+        if (SC == kRow) nxt_sr = p.scales[static_cast<int64_t>(nxt_row) * p.nscale];
       };
       if (pt < kBK) {
         load_row(0);
@@ -780,50 +834,28 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         if (!named_bar_and(2, kProdThreads, ok && wt)) { ok = false; break; }
         if (pt < kBK) {
           s.idx[pt] = nxt_row;
-          s.srow[slot][pt] = nxt_sr;
+          if (SC != kBlock) s.srow[slot][pt] = nxt_sr;
         }
         named_bar_sync(2, kProdThreads);
         // Key quarter q (rows 32q..32q+31) is refilled once PV of block g-NST
-        // has finished with it.
+        // has finished with it: 32 rows x 36 16-byte pieces, consecutive
+        // threads on consecutive pieces of a row, into the SW64 operand
+        // layout.  Blockwise rows land raw (e4m3) in the hi buffer with each
+        // row's block scales in s.bsc; the softmax warps split them.
         for (int q = 0; q < kRowQ; ++q) {
           if (q > 0 && ok) ok = mbar_wait(smem_u32(&s.bar_kv_empty[slot][q]), par, p.err);
           if (!ok) continue;
-          if (KVP == 1) {
-            // 32 rows x 36 16-byte pieces, consecutive threads on consecutive
-            // pieces of a row, into the SW64 operand layout
 #pragma unroll 2
-            for (int i = pt; i < 32 * 36; i += kProdThreads) {
-              const int row = 32 * q + i / 36, c = i % 36;
-              const uint32_t dst = smem_u32(s.kv[slot][0]) + (c >> 2) * kChunkBytes + row * 64 + sw64(row, c & 3);
-              cp_async16_hint(dst, p.latent + static_cast<int64_t>(s.idx[row]) * kD + c * 16, keep);
-            }
-          } else {
-            // blockwise rows: register dequantisation to x * s_blk / s_row, e4m3 hi + lo
-            for (int i = pt; i < 32 * 36; i += kProdThreads) {
-              const int row = 32 * q + i / 36, c = i % 36;
-              const int kc = c >> 2, c4 = c & 3;
-              const uint32_t rr = s.idx[row];
-              uint4 raw;
-              asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-                           : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
-                           : "l"(p.latent + static_cast<int64_t>(rr) * kD + c * 16), "l"(keep));
-              const float ratio = p.scales[static_cast<int64_t>(rr) * p.nscale + (c >> 1)] / s.srow[slot][row];
-              const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-              float x[16];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float2 a = e4m3x2_to_f32x2(static_cast<uint16_t>(wv[k] & 0xffffu));
-                const float2 b = e4m3x2_to_f32x2(static_cast<uint16_t>(wv[k] >> 16));
-                x[4 * k + 0] = a.x * ratio;
-                x[4 * k + 1] = a.y * ratio;
-                x[4 * k + 2] = b.x * ratio;
-                x[4 * k + 3] = b.y * ratio;
-              }
-              uint4 hi, lo;
-              split16(x, hi, lo);
-              const uint32_t off = kc * kChunkBytes + row * 64 + sw64(row, c4);
-              *reinterpret_cast<uint4*>(&s.kv[slot][0][off]) = hi;
-              *reinterpret_cast<uint4*>(&s.kv[slot][KVP - 1][off]) = lo;
+          for (int i = pt; i < 32 * 36; i += kProdThreads) {
+            const int row = 32 * q + i / 36, c = i % 36;
+            const uint32_t dst = smem_u32(s.kv[slot][0]) + (c >> 2) * kChunkBytes + row * 64 + sw64(row, c & 3);
+            cp_async16_hint(dst, p.latent + static_cast<int64_t>(s.idx[row]) * kD + c * 16, keep);
+          }
+          if (KVP == 2) {
+            for (int i = pt; i < 32 * kBlkScales; i += kProdThreads) {
+              const int row = 32 * q + i / kBlkScales, b = i % kBlkScales;
+              cp_async4(smem_u32(&s.bsc[row * kBlkScales + b]),
+                        p.scales + static_cast<int64_t>(s.idx[row]) * p.nscale + b);
             }
           }
         }
@@ -832,7 +864,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
           load_row(j + 1);
           load_scale();
         }
-        if (KVP == 1) cp_async_wait_all();
+        cp_async_wait_all();
         fence_proxy_async_smem();
         mbar_arrive(smem_u32(&s.bar_kv_full[slot]));
       }

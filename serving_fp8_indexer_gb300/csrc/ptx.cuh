@@ -139,6 +139,10 @@ SMLA_DEVICE_INLINE void cp_async16(uint32_t dst, const void* src, uint32_t src_b
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
 }
+// 4-byte global->shared copy (both addresses 4-byte aligned).
+SMLA_DEVICE_INLINE void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
 // Same copy with an L2 eviction-priority policy (from make_policy_evict_last).
 SMLA_DEVICE_INLINE void cp_async16_hint(uint32_t dst, const void* src, uint64_t policy) {
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
@@ -414,6 +418,11 @@ SMLA_DEVICE_INLINE uint32_t f32x2_to_f16x2(float a, float b) {
 SMLA_DEVICE_INLINE uint16_t f16x2_to_e4m3x2(uint32_t v) {
   uint16_t r;
   asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(v));
+  return r;
+}
+SMLA_DEVICE_INLINE uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 SMLA_DEVICE_INLINE uint32_t hsub2(uint32_t a, uint32_t b) {
