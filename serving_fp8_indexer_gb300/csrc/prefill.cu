@@ -133,7 +133,8 @@ struct Smem {
   int mx[kNH];           // block maximum per head (order-preserving ints)
   unsigned long long bar_qraw, bar_q, bar_kv_full[NST], bar_kv_empty[NST][kRowQ];
   unsigned long long bar_s_full, bar_s_free, bar_p_full, bar_pv_done;
-  unsigned long long bar_kv_split;  // blockwise rows: the block's hi / lo terms are written
+  unsigned long long bar_kv_split;         // blockwise rows: the block's hi / lo terms are written
+  unsigned long long bar_kv_q[kRowQ];      // blockwise rows: key quarter q has landed (raw) with s_row
   uint32_t tmem_base;
   int q_issued;  // TMA q loads requested by the QK warp (read at exit)
 };
@@ -189,16 +190,17 @@ __device__ __forceinline__ uint4 quant16(const float (&x)[16]) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Blockwise rows: the softmax warps split a landed block in place.  A piece
-// is 16 bytes (16 e4m3 values) of one row; a warp covers 8 rows x 4 pieces of
-// one 64-byte chunk (512 contiguous bytes: no bank conflicts).  x = e4m3 *
-// (s_blk / s_row) in f16 (the product needs 8 significant bits, f16 keeps
-// 11), hi = x rounded to e4m3's 3 mantissa bits (nearest even, on the f16
-// bits), lo = x - hi (exact); hi overwrites the raw piece, lo goes to the
-// second buffer.  bsc holds 18 block scales per row, then 1 / s_row per row.
-__device__ __forceinline__ void split_block(uint8_t* hi_buf, uint8_t* lo_buf, const float* bsc) {
-  for (int i = threadIdx.x; i < kBK * 36; i += kSoftThreads) {
-    const int kc = i >> 9, row = (i >> 2) & (kBK - 1), c4 = i & 3;
+// Blockwise rows: the softmax warps split a landed key quarter (rows 32q ..
+// 32q + 31) in place.  A piece is 16 bytes (16 e4m3 values) of one row; a
+// warp covers 8 rows x 4 pieces of one 64-byte chunk (512 contiguous bytes:
+// no bank conflicts).  x = e4m3 * (s_blk / s_row) in f16 (the product needs 8
+// significant bits, f16 keeps 11), hi = x rounded to e4m3's 3 mantissa bits
+// (nearest even, on the f16 bits), lo = x - hi (exact); hi overwrites the raw
+// piece, lo goes to the second buffer.  bsc holds 18 block scales per row,
+// then 1 / s_row per row.
+__device__ __forceinline__ void split_quarter(uint8_t* hi_buf, uint8_t* lo_buf, const float* bsc, int q) {
+  for (int i = threadIdx.x; i < 32 * 36; i += kSoftThreads) {
+    const int kc = i >> 7, row = 32 * q + ((i >> 2) & 31), c4 = i & 3;
     const uint32_t off = kc * kChunkBytes + row * 64 + sw64(row, c4);
     const uint4 raw = *reinterpret_cast<const uint4*>(hi_buf + off);
     const float ratio = bsc[row * kBlkScales + 2 * kc + (c4 >> 1)] * bsc[kBK * kBlkScales + row];
@@ -277,6 +279,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const Params p) {
   using S = Smem<QP, KVP, PP, NST>;
   static_assert(!(PP == 2 && KVP == 2), "P lo has a buffer only when rows are single-term");
+  static_assert(KVP == 1 || NST == 1, "the blockwise quarter barriers complete once per block (one slot)");
   static_assert(offsetof(S, kv) % 1024 == 0 && offsetof(S, plo) % 1024 == 0,
                 "swizzled operand tiles need 1024-byte alignment");
   static_assert(offsetof(S, cs) % 16 == 0 && offsetof(S, negm) % 16 == 0, "cs / negm are read as float4");
@@ -314,6 +317,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     mbar_init(smem_u32(&s.bar_p_full), kSoftThreads);
     mbar_init(smem_u32(&s.bar_pv_done), 1);
     mbar_init(smem_u32(&s.bar_kv_split), kSoftThreads);
+    for (int q = 0; q < kRowQ; ++q) mbar_init(smem_u32(&s.bar_kv_q[q]), kProdThreads);
     fence_mbar_init();
     tma_prefetch_desc(&tq);
   }
@@ -450,24 +454,20 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         const int slot = g % NST;
         // S^T of block j is ready; kv_full is also waited so that the
         // producers' per-row scales are visible to this thread.
-        bool wt = mbar_wait(smem_u32(&s.bar_kv_full[slot]), (g / NST) & 1, p.err);
+        bool wt = true;
         if (KVP == 2) {
-          // Blockwise rows landed raw: s_row = the row's largest block scale
-          // (1 if none is positive), then in place x * s_blk / s_row -> e4m3
-          // hi (over the raw piece) + lo, released to QK by kv_split.
-          if (!named_bar_and(1, kSoftThreads, wt)) { ok = false; break; }
-          if (threadIdx.x < kBK) {
-            float sr = 0.f;
-#pragma unroll
-            for (int b = 0; b < kBlkScales; ++b) sr = fmaxf(sr, s.bsc[threadIdx.x * kBlkScales + b]);
-            sr = sr > 0.f ? sr : 1.f;
-            s.srow[slot][threadIdx.x] = sr;
-            s.bsc[kBK * kBlkScales + threadIdx.x] = 1.f / sr;
+          // Blockwise rows land raw, key quarter by key quarter, each with its
+          // rows' s_row: split each quarter in place as it lands, then
+          // release the block to QK.
+#pragma unroll 1
+          for (int q = 0; q < kRowQ; ++q) {
+            wt = wt && mbar_wait(smem_u32(&s.bar_kv_q[q]), g & 1, p.err);
+            if (wt) split_quarter(s.kv[slot][0], s.kv[slot][KVP - 1], s.bsc, q);
           }
-          named_bar_sync(1, kSoftThreads);
-          split_block(s.kv[slot][0], s.kv[slot][KVP - 1], s.bsc);
           fence_proxy_async_smem();
           mbar_arrive(smem_u32(&s.bar_kv_split));
+        } else {
+          wt = mbar_wait(smem_u32(&s.bar_kv_full[slot]), (g / NST) & 1, p.err);
         }
         wt = wt && mbar_wait(smem_u32(&s.bar_s_full), g & 1, p.err);
         if (!named_bar_and(1, kSoftThreads, wt)) { ok = false; break; }
@@ -840,22 +840,44 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         // Key quarter q (rows 32q..32q+31) is refilled once PV of block g-NST
         // has finished with it: 32 rows x 36 16-byte pieces, consecutive
         // threads on consecutive pieces of a row, into the SW64 operand
-        // layout.  Blockwise rows land raw (e4m3) in the hi buffer with each
-        // row's block scales in s.bsc; the softmax warps split them.
+        // layout.  Blockwise rows land raw (e4m3) in the hi buffer, and the
+        // row's 18 block scales (one thread per row) in s.bsc; each quarter is
+        // published (kv_q) once landed, with s_row and 1 / s_row of its rows,
+        // and the softmax warps split it while later quarters land (measured:
+        // publishing only after all four quarters were issued was slower).
+        auto publish_quarter = [&](int qq) {
+          if (pt < 32) {
+            const int row = 32 * qq + pt;
+            float sr = 0.f;
+#pragma unroll
+            for (int b = 0; b < kBlkScales; ++b) sr = fmaxf(sr, s.bsc[row * kBlkScales + b]);
+            sr = sr > 0.f ? sr : 1.f;
+            s.srow[slot][row] = sr;
+            s.bsc[kBK * kBlkScales + row] = 1.f / sr;
+          }
+          mbar_arrive(smem_u32(&s.bar_kv_q[qq]));
+        };
         for (int q = 0; q < kRowQ; ++q) {
           if (q > 0 && ok) ok = mbar_wait(smem_u32(&s.bar_kv_empty[slot][q]), par, p.err);
-          if (!ok) continue;
+          if (ok) {
 #pragma unroll 2
-          for (int i = pt; i < 32 * 36; i += kProdThreads) {
-            const int row = 32 * q + i / 36, c = i % 36;
-            const uint32_t dst = smem_u32(s.kv[slot][0]) + (c >> 2) * kChunkBytes + row * 64 + sw64(row, c & 3);
-            cp_async16_hint(dst, p.latent + static_cast<int64_t>(s.idx[row]) * kD + c * 16, keep);
+            for (int i = pt; i < 32 * 36; i += kProdThreads) {
+              const int row = 32 * q + i / 36, c = i % 36;
+              const uint32_t dst = smem_u32(s.kv[slot][0]) + (c >> 2) * kChunkBytes + row * 64 + sw64(row, c & 3);
+              cp_async16_hint(dst, p.latent + static_cast<int64_t>(s.idx[row]) * kD + c * 16, keep);
+            }
+            if (KVP == 2 && pt < 32) {
+              const int row = 32 * q + pt;
+              const float* src = p.scales + static_cast<int64_t>(s.idx[row]) * p.nscale;
+#pragma unroll
+              for (int b = 0; b < kBlkScales; ++b) cp_async4(smem_u32(&s.bsc[row * kBlkScales + b]), src + b);
+            }
           }
-          if (KVP == 2) {
-            for (int i = pt; i < 32 * kBlkScales; i += kProdThreads) {
-              const int row = 32 * q + i / kBlkScales, b = i % kBlkScales;
-              cp_async4(smem_u32(&s.bsc[row * kBlkScales + b]),
-                        p.scales + static_cast<int64_t>(s.idx[row]) * p.nscale + b);
+          if (KVP == 2) {  // quarter q - 1 is published once it has landed, while q is in flight
+            cp_async_commit();
+            if (q > 0) {
+              cp_async_wait_group<1>();
+              publish_quarter(q - 1);
             }
           }
         }
@@ -865,8 +887,12 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
           load_scale();
         }
         cp_async_wait_all();
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&s.bar_kv_full[slot]));
+        if (KVP == 2) {
+          publish_quarter(kRowQ - 1);
+        } else {
+          fence_proxy_async_smem();
+          mbar_arrive(smem_u32(&s.bar_kv_full[slot]));
+        }
       }
       gb += I.nblk;
     }
