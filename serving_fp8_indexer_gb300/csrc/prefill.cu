@@ -181,6 +181,16 @@ __device__ __forceinline__ void split8(const float (&x)[8], uint2& hi, uint2& lo
   hi = make_uint2(h[0], h[1]);
   lo = make_uint2(l[0], l[1]);
 }
+// Splits f16x2 a into e4m3 hi + lo: hi = a rounded to e4m3's 3 mantissa
+// bits (nearest even, as integer operations on the f16 bits; exact in e4m3's
+// normal range), lo = a - hi (exact in f16).  Two conversions per pair.  (For
+// the softmax's P and the q split, where the issue rate binds rather than the
+// conversion rate, the conversion round trip in split16 / split8 measured faster.)
+__device__ __forceinline__ void split_f16x2(uint32_t a, uint16_t& hi, uint16_t& lo) {
+  const uint32_t h = (a + 0x003f003fu + ((a >> 7) & 0x00010001u)) & 0xff80ff80u;
+  hi = f16x2_to_e4m3x2(h);
+  lo = f16x2_to_e4m3x2(hsub2(a, h));
+}
 __device__ __forceinline__ uint4 quant16(const float (&x)[16]) {
   uint32_t w[4];
 #pragma unroll
@@ -196,8 +206,8 @@ __device__ __forceinline__ uint4 quant16(const float (&x)[16]) {
 // no bank conflicts).  x = e4m3 * (s_blk / s_row) in f16 (the product needs 8
 // significant bits, f16 keeps 11), hi = x rounded to e4m3's 3 mantissa bits
 // (nearest even, on the f16 bits), lo = x - hi (exact); hi overwrites the raw
-// piece, lo goes to the second buffer.  bsc holds 18 block scales per row,
-// then 1 / s_row per row.
+// piece, lo goes to the second buffer (split_f16x2).  bsc holds 18 block
+// scales per row, then 1 / s_row per row.
 __device__ __forceinline__ void split_quarter(uint8_t* hi_buf, uint8_t* lo_buf, const float* bsc, int q) {
   for (int i = threadIdx.x; i < 32 * 36; i += kSoftThreads) {
     const int kc = i >> 7, row = 32 * q + ((i >> 2) & 31), c4 = i & 3;
@@ -209,15 +219,11 @@ __device__ __forceinline__ void split_quarter(uint8_t* hi_buf, uint8_t* lo_buf, 
     uint32_t h[4], l[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      uint32_t xh[2], hh[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        xh[u] = hmul2(e4m3x2_to_f16x2(static_cast<uint16_t>(u == 0 ? wv[k] & 0xffffu : wv[k] >> 16)), r2);
-        hh[u] = (xh[u] + 0x003f003fu + ((xh[u] >> 7) & 0x00010001u)) & 0xff80ff80u;
-      }
-      h[k] = static_cast<uint32_t>(f16x2_to_e4m3x2(hh[0])) | (static_cast<uint32_t>(f16x2_to_e4m3x2(hh[1])) << 16);
-      l[k] = static_cast<uint32_t>(f16x2_to_e4m3x2(hsub2(xh[0], hh[0]))) |
-             (static_cast<uint32_t>(f16x2_to_e4m3x2(hsub2(xh[1], hh[1]))) << 16);
+      uint16_t ha, hb, la, lb;
+      split_f16x2(hmul2(e4m3x2_to_f16x2(static_cast<uint16_t>(wv[k] & 0xffffu)), r2), ha, la);
+      split_f16x2(hmul2(e4m3x2_to_f16x2(static_cast<uint16_t>(wv[k] >> 16)), r2), hb, lb);
+      h[k] = static_cast<uint32_t>(ha) | (static_cast<uint32_t>(hb) << 16);
+      l[k] = static_cast<uint32_t>(la) | (static_cast<uint32_t>(lb) << 16);
     }
     *reinterpret_cast<uint4*>(hi_buf + off) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4*>(lo_buf + off) = make_uint4(l[0], l[1], l[2], l[3]);
