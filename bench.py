@@ -46,6 +46,18 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def dtype_label(w):
+    """The arithmetic the path runs in, per workload."""
+    from serving_fp8_indexer_gb300 import workloads as wl
+    if not w.H:
+        return "e4m3 MMA (indexer q and k), f32 accumulate"
+    if w.q_dtype == wl.Q_E4M3 and 0 < w.scale_block_size < 576:
+        return "e4m3 MMA (e4m3 q; blockwise rows re-expressed as e4m3 hi+lo; P e4m3), f32 accumulate"
+    if w.q_dtype == wl.Q_E4M3:
+        return "e4m3 MMA (e4m3 q, e4m3 rows, P e4m3), f32 accumulate"
+    return "e4m3 MMA (bf16 q and P as e4m3 hi+lo), f32 accumulate"
+
+
 def profiled_traffic(kernel_src, profile_md, captured_tokens, tokens):
     """DRAM bytes per launch from a committed ncu summary (read + write of a
     smaller launch of the same kernel variant), scaled by the tokens a launch
@@ -147,6 +159,8 @@ CASES = {
     "mtp_decode": ("mtp_decode_indexer", dict()),
     "dsv32": ("dsv32_prefill", dict()),
     "blockwise": ("blockwise_fp8_prefill", dict()),
+    # two of its four sequences (3072 tokens), for ncu captures
+    "blockwise_small": ("blockwise_fp8_prefill", dict(lens=(1024, 2048))),
 }
 
 
@@ -401,6 +415,11 @@ def run_ours(args, rank, world):
     peaks, src = load_peaks()
     bf16_peak = peak_value(peaks, "bf16_tflops_sustained")
     hbm = peak_value(peaks, "hbm_gbs")
+    # the attention's tensor peak is that of the method's dtype: bf16 for bf16 q,
+    # FP8 (2 x the bf16 figure, the nominal ratio) for e4m3 q
+    fp8_q = w.q_dtype == wl.Q_E4M3
+    attn_peak = 2.0 * bf16_peak if fp8_q else bf16_peak
+    attn_peak_name = "fp8 dense = 2 x bf16 (sustained)" if fp8_q else "bf16 dense (sustained)"
     stages = {}
     if "indexer" in stage:
         idx_bytes = w.q_idx.nbytes + w.q_scale.nbytes + w.k_pool.nbytes + w.k_scale.nbytes + 4 * kt
@@ -411,7 +430,8 @@ def run_ours(args, rank, world):
         stages["topk"] = {"ms": stage["topk"], "GB/s_algorithmic": gbs, "frac_hbm": gbs / hbm}
     if "sparse_mla" in stage:
         tf = flops / (stage["sparse_mla"] * 1e-3) / 1e12
-        stages["sparse_mla"] = {"ms": stage["sparse_mla"], "TFLOP/s": tf, "frac_bf16_peak": tf / bf16_peak}
+        stages["sparse_mla"] = {"ms": stage["sparse_mla"], "TFLOP/s": tf, "frac_peak": tf / attn_peak,
+                                "peak_dtype": "fp8" if fp8_q else "bf16"}
     if has_attn:
         value, unit = world * flops / (ms_step * 1e-3) / 1e12, "TFLOP/s"
     else:
@@ -427,7 +447,7 @@ def run_ours(args, rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3 MMA (bf16 q and P as e4m3 hi+lo), f32 accumulate",
+        "dtype": dtype_label(w),
         "data": "synthetic",
         "config": config_dict(w, world),
         "stages": stages,
@@ -447,9 +467,12 @@ def run_ours(args, rank, world):
         if args.case in ("chunk", "chunk_small"):
             traffic = profiled_traffic("serving_fp8_indexer_gb300/csrc/prefill.cu",
                                        "profiles/prefill_kernel_chunk_small.md", 1024, int(w.seqs.T))
+        elif args.case in ("blockwise", "blockwise_small"):
+            traffic = profiled_traffic("serving_fp8_indexer_gb300/csrc/prefill.cu",
+                                       "profiles/prefill_kernel_blockwise_small.md", 3072, int(w.seqs.T))
         line["roofline"] = {"bound": "tensor", "kernel": "prefill_kernel (sparse MLA)", "achieved": tf,
-                            "peak": bf16_peak, "unit": "TFLOP/s", "frac": tf / bf16_peak, "traffic": traffic,
-                            "peak_source": f"{src} bf16 dense (sustained)"}
+                            "peak": attn_peak, "unit": "TFLOP/s", "frac": tf / attn_peak, "traffic": traffic,
+                            "peak_source": f"{src} {attn_peak_name}"}
     elif "topk" in stage:
         line["roofline"] = {"bound": "hbm", "kernel": "topk_kernel", "achieved": stages["topk"]["GB/s_algorithmic"],
                             "peak": hbm, "unit": "GB/s", "frac": stages["topk"]["frac_hbm"], "traffic": None,
