@@ -203,8 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int key0 = kt * kBM + bx * p.box_rows;
           rows[bx] = -1;
           if (key0 >= kvl) continue;
-          const int page = key0 / p.page_size;
-          const int pid = page < p.max_pages ? p.page_table[static_cast<int64_t>(b) * p.max_pages + page] : -1;
+          // the item's page ids are staged in shared memory (no L2 round trip per box)
+          const int pi = (key0 >> p.page_shift) - page_lo;
+          const int pid = pi < npg ? s.pages[pi] : -1;
           const int64_t row = static_cast<int64_t>(pid) * p.page_size + key0 % p.page_size;
           if (pid < 0 || row + p.box_rows > p.phys_rows) {
             atomicOr(p.err, kErrPage);
