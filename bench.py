@@ -301,19 +301,23 @@ def run_ours(args, rank, world):
     stream = torch.cuda.current_stream(dev)
     n_kernels = (2 if has_idx else 0) + (1 if has_attn else 0)
 
-    def step(ev=None):
-        i = 0
+    def step(ev=None, tin=None, o=None):
+        # tin / o: the step's input tensors and result (attention output, or
+        # the top-k indices for indexer-only workloads); default the bench's own
+        tin = t_in if tin is None else tin
+        o_idx = o if (o is not None and not has_attn) else idx
+        o_out = o if (o is not None and has_attn) else (out if has_attn else None)
         if ev is not None:
             ev[0].record(stream)
         if has_idx:
-            smla.indexer_scores(t_in["q_idx"], t_in["q_scale"], k_pool, k_scale, seqs, scores)
+            smla.indexer_scores(tin["q_idx"], tin["q_scale"], k_pool, k_scale, seqs, scores)
             if ev is not None:
                 ev[1].record(stream)
-            smla.topk(scores, seqs, k, idx, lens)
+            smla.topk(scores, seqs, k, o_idx, lens)
             if ev is not None:
                 ev[2].record(stream)
         if has_attn:
-            smla.sparse_prefill(t_in["q_attn"], latent, scales, w.scale_block_size, idx, lens, w.softmax_scale, out)
+            smla.sparse_prefill(tin["q_attn"], latent, scales, w.scale_block_size, o_idx, lens, w.softmax_scale, o_out)
             if ev is not None:
                 ev[3].record(stream)
 
@@ -373,33 +377,63 @@ def run_ours(args, rank, world):
             stage[x] = float(t[i + 1])
     ms_step = total_ms / args.steps
 
-    # ---- end to end through the C ABI with host buffers (pinned), copies timed
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed.
+    # Serving-style pipeline: every step copies its inputs in from pinned host
+    # memory and its result back out, on copy streams of their own, into two
+    # device buffer sets used in turn, so step i's copies overlap the compute
+    # of steps i - 1 and i + 1 (each step's copies stay inside the timed region).
     e2e = None
     if not args.no_e2e:
         host = {name: (torch.from_numpy(w.q_attn.view(np.int16)).view(torch.bfloat16) if name == "q_attn" and
                        w.q_dtype == wl.Q_BF16 else
                        torch.from_numpy({"q_idx": w.q_idx, "q_scale": w.q_scale, "q_attn": w.q_attn}[name])).pin_memory()
                 for name in t_in}
+        res0 = out if has_attn else idx
         h_out = (torch.empty((T, H, 512), dtype=torch.bfloat16) if has_attn else
                  torch.empty((T, k), dtype=torch.int32)).pin_memory()
-        n_e2e = max(1, min(args.steps, 5))
+        sets = [(t_in, res0), ({name: torch.empty_like(x) for name, x in t_in.items()}, torch.empty_like(res0))]
+        h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        in_ready = [torch.cuda.Event() for _ in range(2)]
+        in_free = [torch.cuda.Event() for _ in range(2)]
+        out_ready = [torch.cuda.Event() for _ in range(2)]
+        out_free = [torch.cuda.Event() for _ in range(2)]
+        for b in range(2):  # all buffers start free
+            in_free[b].record(stream)
+            out_free[b].record(stream)
+        n_e2e = max(4, min(args.steps, 8))
 
-        def e2e_step():
-            for name, ht in host.items():
-                t_in[name].copy_(ht, non_blocking=True)
-            step()
-            h_out.copy_(out if has_attn else idx.view(torch.int32), non_blocking=True)
+        def e2e_step(i):
+            b = i % 2
+            tin, res = sets[b]
+            with torch.cuda.stream(h2d):
+                h2d.wait_event(in_free[b])
+                for name, ht in host.items():
+                    tin[name].copy_(ht, non_blocking=True)
+                in_ready[b].record(h2d)
+            stream.wait_event(in_ready[b])
+            stream.wait_event(out_free[b])
+            step(tin=tin, o=res)
+            in_free[b].record(stream)
+            out_ready[b].record(stream)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(out_ready[b])
+                h_out.copy_(res if has_attn else res.view(torch.int32), non_blocking=True)
+                out_free[b].record(d2h)
 
-        e2e_step()
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize(dev)
         a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
+        b_ev = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        b.record(stream)
+        h2d.wait_event(a)
+        d2h.wait_event(a)
+        for i in range(n_e2e):
+            e2e_step(i)
+        stream.wait_stream(d2h)  # the last result is back on the host
+        b_ev.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = a.elapsed_time(b) / n_e2e
+        e2e_ms = a.elapsed_time(b_ev) / n_e2e
         if world > 1:
             t = torch.tensor([e2e_ms], device=dev)
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
