@@ -5,8 +5,9 @@
 // head h and the n = topk_lengths[t] gathered latent rows K_j,
 //   out[t,h,:] = sum_j softmax_j(softmax_scale * q[t,h] . K_j) * K_j[0:512].
 //
-// GB300 design.  One CTA per (token, group of 64 heads); the token's keys
-// are processed in blocks of 128 gathered rows.  The block's keys are the
+// GB300 design.  A work item is (token, group of 64 heads); persistent CTAs
+// (one per SM) take the items in turn, and an item's keys are processed in
+// blocks of 128 gathered rows.  The block's keys are the
 // MMA M dimension and the heads the N dimension:
 //   S^T[128 keys x 64 heads] = K_blk . Q^T           (TMEM, 64 columns)
 //   O^T[512 vcols x 64 heads] += V_blk^T . P^T       (TMEM, 4 x 64 columns)
@@ -16,14 +17,14 @@
 // read MN-major (V = the first 512 columns of K).
 //
 // All products run on the FP8 pipe (kind::f8f6f4, f32 accumulation):
-//   * e4m3 q is used as is; bf16 q is split once per CTA into two e4m3
+//   * e4m3 q is used as is; bf16 q is split once per item into two e4m3
 //     terms q*2^e = hi + lo (per-head power-of-two 2^e keeps lo in range),
 //     both multiplied into the same S accumulator (error ~2^-8 relative);
 //   * P is quantised to one e4m3 term (native FP8-P path) or, for the bf16
 //     path, to hi + lo like q;
-//   * blockwise-scaled rows (32-wide scales) are dequantised in registers
-//     during the gather to x * s_blk / s_row and stored as e4m3 hi + lo,
-//     after which every row carries one scale s_row.
+//   * blockwise-scaled rows (32-wide scales) are gathered raw with their
+//     block scales and split in shared memory into e4m3 hi + lo of
+//     x * s_blk / s_row, after which every row carries one scale s_row.
 // A per-row scale s_j (tensorwise, or s_row) enters exactly: the logit is
 // z = acc * s_j * c_h, the PV operand is exp2(z + log2 s_j - m) and the
 // normaliser sums exp2(z - m), so out = sum_j p_j s_j Vraw_j / sum_j p_j.
@@ -52,7 +53,7 @@
 // Warp roles (24 warps): warps 0-7 softmax / epilogue (lane quarter w%4,
 // head half w/4; thread = one key x 32 heads), warp 8 QK issuer and TMEM
 // owner, warp 9 PV issuer, warps 10-23 gather producers (cp.async 16 B into
-// the SW64 layout, or a register dequantisation of blockwise rows).
+// the SW64 layout; for blockwise rows also the block scales).
 #include <algorithm>
 #include <cstddef>
 
@@ -812,8 +813,8 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
       if (n == 0) continue;
       const uint32_t* tok_idx = p.indices + static_cast<int64_t>(I.t) * p.indices_stride;
       const uint32_t first = tok_idx[0];
-      // Thread pt < 128 owns row pt of every block: its physical row and
-      // scale are loaded one block ahead.
+      // Thread pt < 128 owns row pt of every block: its physical row (and
+      // tensorwise scale) are loaded one block ahead.
       uint32_t nxt_row = 0;
       float nxt_sr = 1.f;
       auto load_row = [&](int jb) {

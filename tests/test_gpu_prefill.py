@@ -54,9 +54,18 @@ def test_bf16_tensorwise_chunk_end_to_end():
     _end_to_end(wl.e2e_chunk(B=2, L=600, q_len=200, k=256, H=128, h_idx=64))
 
 
-@pytest.mark.parametrize("H", [16, 32, 192, 256])
+@pytest.mark.parametrize("H", [16, 32, 48, 192, 256])
 def test_head_counts(H):
     w = wl.build(f"h{H}", 40 + H, [70], [200], 64, topk=130, H=H, q_dtype=wl.Q_BF16, sbs=0, sample_indices=True)
+    _sampled(w)
+
+
+@pytest.mark.parametrize("H", [16, 48])
+def test_fp8_q_partial_head_group(H):
+    # e4m3 q with fewer than 64 heads: the q tile's rows past the group belong
+    # to the next token (or lie past the tensor) and must not leak in
+    w = wl.build(f"fp8_h{H}", 60 + H, [90, 33], [150, 40], 64, topk=140, H=H, q_dtype=wl.Q_E4M3, sbs=576,
+                 sample_indices=True)
     _sampled(w)
 
 
