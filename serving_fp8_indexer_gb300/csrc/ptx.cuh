@@ -58,16 +58,6 @@ SMLA_DEVICE_INLINE bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Non-blocking test of the phase with the given parity.
-SMLA_DEVICE_INLINE bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 // Waits for the phase with the given parity to complete.  Gives up after
 // kWaitLimitNs, records kErrTimeout and returns false.
 SMLA_DEVICE_INLINE bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
@@ -134,11 +124,6 @@ SMLA_DEVICE_INLINE bool named_bar_and(int id, int nthreads, bool pred) {
 }
 
 // ------------------------------------------------------------------ cp.async
-// 16-byte global->shared copy; src_bytes < 16 zero-fills the rest (0 reads nothing).
-SMLA_DEVICE_INLINE void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
 // 4-byte global->shared copy (both addresses 4-byte aligned).
 SMLA_DEVICE_INLINE void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
@@ -160,8 +145,6 @@ SMLA_DEVICE_INLINE uint64_t make_policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
-// 16-byte streaming global load (cache-streaming: evicted first).
-SMLA_DEVICE_INLINE uint4 ld_stream16(const void* p) { return __ldcs(reinterpret_cast<const uint4*>(p)); }
 SMLA_DEVICE_INLINE void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 SMLA_DEVICE_INLINE void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Waits until at most N of this thread's committed cp.async groups are pending.
@@ -204,16 +187,6 @@ SMLA_DEVICE_INLINE void tma_load_3d_hint(uint32_t dst, const CUtensorMap* m, int
       : "memory");
 }
 
-// Four rows (y0..y3) x one box of columns starting at x, gathered into four
-// consecutive box-rows of shared memory (tensor map box = [box_x, 1]).
-SMLA_DEVICE_INLINE void tma_gather4_2d(uint32_t dst, const CUtensorMap* m, int x, int y0, int y1, int y2, int y3,
-                                       uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-      : "memory");
-}
 
 // ------------------------------------------------------------------ tcgen05
 // Allocates `ncols` TMEM columns (power of two >= 32); the whole warp calls.
@@ -237,16 +210,6 @@ SMLA_DEVICE_INLINE void mma_f8f6f4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f8f6f4 (A K-major in TMEM: lane =
-// row, four 8-bit elements per 32-bit column), issued by one thread.
-SMLA_DEVICE_INLINE void mma_f8f6f4_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                      uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Arrives (once) on `bar` when every tcgen05 op issued so far by this thread completes.
@@ -286,89 +249,9 @@ SMLA_DEVICE_INLINE void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
       "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
-SMLA_DEVICE_INLINE void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
-      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
 
-SMLA_DEVICE_INLINE void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
-               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
-}
-SMLA_DEVICE_INLINE void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(r[0]), "r"(r[1]),
-               "r"(r[2]), "r"(r[3])
-               : "memory");
-}
 
-// ------------------------------------------------------------------ clusters
-SMLA_DEVICE_INLINE uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Address of the same shared-memory location in CTA `rank` of the cluster.
-SMLA_DEVICE_INLINE uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-SMLA_DEVICE_INLINE void st_cluster_v4(uint32_t addr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-// Arrive on an mbarrier of another CTA of the cluster (release, cluster scope).
-SMLA_DEVICE_INLINE void mbar_arrive_cluster(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
-}
-SMLA_DEVICE_INLINE bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait with cluster-scope acquire (sees the peer's remote stores).
-SMLA_DEVICE_INLINE bool mbar_wait_cluster(uint32_t bar, uint32_t parity, unsigned* err) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const unsigned long long t0 = global_timer_ns();
-  while (true) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(err, kErrTimeout);
-      return false;
-    }
-  }
-}
-// Bulk copy (no tensor map) of `bytes` (a multiple of 16, both addresses
-// 16-byte aligned) from this CTA's shared memory to global memory, in a
-// bulk async-group of the issuing thread.  The source must have been made
-// visible to the async proxy (fence.proxy.async after the writes).
-SMLA_DEVICE_INLINE void bulk_store_s2g(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-               : "memory");
-}
-SMLA_DEVICE_INLINE void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Waits until every bulk group of this thread has read its shared-memory
-// source (the global writes complete asynchronously, before the kernel ends).
-SMLA_DEVICE_INLINE void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
-SMLA_DEVICE_INLINE void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
 // stride byte offsets (16-byte units), descriptor version 1, swizzle mode
@@ -435,11 +318,6 @@ SMLA_DEVICE_INLINE uint32_t e4m3x2_to_f16x2(uint16_t v) {
   uint32_t r;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
   return r;
-}
-SMLA_DEVICE_INLINE float2 e4m3x2_to_f32x2(uint16_t v) {
-  const uint32_t h = e4m3x2_to_f16x2(v);
-  __half2 hh = *reinterpret_cast<const __half2*>(&h);
-  return __half22float2(hh);
 }
 
 }  // namespace smla
