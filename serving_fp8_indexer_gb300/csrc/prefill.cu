@@ -210,24 +210,40 @@ __device__ __forceinline__ uint4 quant16(const float (&x)[16]) {
 // piece, lo goes to the second buffer (split_f16x2).  bsc holds 18 block
 // scales per row, then 1 / s_row per row.
 __device__ __forceinline__ void split_quarter(uint8_t* hi_buf, uint8_t* lo_buf, const float* bsc, int q) {
-  for (int i = threadIdx.x; i < 32 * 36; i += kSoftThreads) {
-    const int kc = i >> 7, row = 32 * q + ((i >> 2) & 31), c4 = i & 3;
-    const uint32_t off = kc * kChunkBytes + row * 64 + sw64(row, c4);
-    const uint4 raw = *reinterpret_cast<const uint4*>(hi_buf + off);
-    const float ratio = bsc[row * kBlkScales + 2 * kc + (c4 >> 1)] * bsc[kBK * kBlkScales + row];
-    const uint32_t r2 = f32x2_to_f16x2(ratio, ratio);
-    const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t h[4], l[4];
+  // All of a thread's pieces are read first, then converted and written, so
+  // that their conversion chains interleave (a piece is only ever read and
+  // rewritten by its own thread).
+  constexpr int kIt = (32 * 36 + kSoftThreads - 1) / kSoftThreads;
+  uint4 raw[kIt];
+  uint32_t off[kIt];
+  float ratio[kIt];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint16_t ha, hb, la, lb;
-      split_f16x2(hmul2(e4m3x2_to_f16x2(static_cast<uint16_t>(wv[k] & 0xffffu)), r2), ha, la);
-      split_f16x2(hmul2(e4m3x2_to_f16x2(static_cast<uint16_t>(wv[k] >> 16)), r2), hb, lb);
-      h[k] = static_cast<uint32_t>(ha) | (static_cast<uint32_t>(hb) << 16);
-      l[k] = static_cast<uint32_t>(la) | (static_cast<uint32_t>(lb) << 16);
+  for (int it = 0; it < kIt; ++it) {
+    const int i = threadIdx.x + it * kSoftThreads;
+    if (i < 32 * 36) {
+      const int kc = i >> 7, row = 32 * q + ((i >> 2) & 31), c4 = i & 3;
+      off[it] = kc * kChunkBytes + row * 64 + sw64(row, c4);
+      raw[it] = *reinterpret_cast<const uint4*>(hi_buf + off[it]);
+      ratio[it] = bsc[row * kBlkScales + 2 * kc + (c4 >> 1)] * bsc[kBK * kBlkScales + row];
     }
-    *reinterpret_cast<uint4*>(hi_buf + off) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(lo_buf + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+#pragma unroll
+  for (int it = 0; it < kIt; ++it) {
+    if (threadIdx.x + it * kSoftThreads < 32 * 36) {
+      const uint32_t r2 = f32x2_to_f16x2(ratio[it], ratio[it]);
+      const uint32_t wv[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
+      uint32_t h[4], l[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint16_t ha, hb, la, lb;
+        split_f16x2(hmul2(e4m3x2_to_f16x2(static_cast<uint16_t>(wv[k] & 0xffffu)), r2), ha, la);
+        split_f16x2(hmul2(e4m3x2_to_f16x2(static_cast<uint16_t>(wv[k] >> 16)), r2), hb, lb);
+        h[k] = static_cast<uint32_t>(ha) | (static_cast<uint32_t>(hb) << 16);
+        l[k] = static_cast<uint32_t>(la) | (static_cast<uint32_t>(lb) << 16);
+      }
+      *reinterpret_cast<uint4*>(hi_buf + off[it]) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(lo_buf + off[it]) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
   }
 }
 
