@@ -46,6 +46,23 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def max_over_ranks(values, device):
+    """Each timing's maximum over all ranks (the slowest replica sets the step
+    time); values unchanged on one rank."""
+    import torch
+    if not torch.distributed.is_available() or not torch.distributed.is_initialized() or \
+            torch.distributed.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def weak_scaling_value(world, work_per_rank, ms_per_step):
+    """Whole-job throughput when every rank processes the same work per step."""
+    return world * work_per_rank / (ms_per_step * 1e-3)
+
+
 def dtype_label(w):
     """The arithmetic the path runs in, per workload."""
     from serving_fp8_indexer_gb300 import workloads as wl
@@ -370,11 +387,10 @@ def run_ours(args, rank, world):
             stage["sparse_mla"] = statistics.mean(e[a].elapsed_time(e[3]) for e in evs)
     if world > 1:
         keys = sorted(stage)
-        t = torch.tensor([total_ms] + [stage[x] for x in keys], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t[0])
+        red = max_over_ranks([total_ms] + [stage[x] for x in keys], dev)
+        total_ms = red[0]
         for i, x in enumerate(keys):
-            stage[x] = float(t[i + 1])
+            stage[x] = red[i + 1]
     ms_step = total_ms / args.steps
 
     # ---- end to end through the C ABI with host buffers (pinned), copies timed.
@@ -435,12 +451,10 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize(dev)
         e2e_ms = a.elapsed_time(b_ev) / n_e2e
         if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+            e2e_ms = max_over_ranks([e2e_ms], dev)[0]
         bi = sum(ht.numel() * ht.element_size() for ht in host.values())
         bo = h_out.numel() * h_out.element_size()
-        ev = world * (flops if has_attn else kt) / (e2e_ms * 1e-3)
+        ev = weak_scaling_value(world, flops if has_attn else kt, e2e_ms)
         e2e = {"value": ev / 1e12 if has_attn else ev, "unit": "TFLOP/s" if has_attn else "keys·tok/s",
                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo), "ms_per_step": e2e_ms}
 
@@ -467,9 +481,9 @@ def run_ours(args, rank, world):
         stages["sparse_mla"] = {"ms": stage["sparse_mla"], "TFLOP/s": tf, "frac_peak": tf / attn_peak,
                                 "peak_dtype": "fp8" if fp8_q else "bf16"}
     if has_attn:
-        value, unit = world * flops / (ms_step * 1e-3) / 1e12, "TFLOP/s"
+        value, unit = weak_scaling_value(world, flops, ms_step) / 1e12, "TFLOP/s"
     else:
-        value, unit = world * kt / (ms_step * 1e-3), "keys·tok/s"
+        value, unit = weak_scaling_value(world, kt, ms_step), "keys·tok/s"
     line = {
         "metric": METRIC,
         "value": value,
