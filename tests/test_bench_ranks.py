@@ -52,3 +52,22 @@ def test_reference_arm_other_ranks_do_nothing():
         pass
     # ranks other than 0 return at once without touching the oracle
     assert bench.run_reference(A(), 1, 2) is None
+
+
+def test_profiled_traffic_reads_the_committed_capture(tmp_path):
+    # the committed capture of the current kernel source parses to read + write
+    # bytes scaled by tokens; another source (sha1 mismatch) gives None
+    t = bench.profiled_traffic("serving_fp8_indexer_gb300/csrc/prefill.cu",
+                               "profiles/prefill_kernel_chunk_small.md", 1024, 16384)
+    assert t is not None and 3.0e9 < t < 5.0e9
+    md = tmp_path / "p.md"
+    md.write_text("sha1 0000\n| `dram__bytes_read.sum` / `dram__bytes_write.sum` | 1.0 MB / 2.0 MB |\n")
+    assert bench.profiled_traffic("serving_fp8_indexer_gb300/csrc/prefill.cu", str(md), 1, 2) is None
+
+
+def test_dtype_labels_follow_the_workload():
+    from serving_fp8_indexer_gb300 import workloads as wl
+    assert "bf16 q" in bench.dtype_label(bench.make_workload("tiny"))
+    assert "blockwise" in bench.dtype_label(bench.make_workload("blockwise_small"))
+    assert "indexer" in bench.dtype_label(bench.make_workload("mtp_decode"))
+    assert wl.Q_E4M3 != wl.Q_BF16
