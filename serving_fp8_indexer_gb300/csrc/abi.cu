@@ -47,8 +47,8 @@ bool encode_tma_u8(CUtensorMap* map, const void* base, int rank, const uint64_t*
     estr[i] = 1;
     if (i + 1 < rank) st[i] = strides[i];
   }
-  // The driver entry point is looked up through the runtime, so the library
-  // does not link libcuda directly (it loads on machines without a driver).
+  // The CUDA driver entry point is looked up through the runtime, so the library
+  // does not link libcuda directly (it loads on machines without a CUDA driver).
   using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);

@@ -15,7 +15,7 @@ smla_status_t fail_cuda(cudaError_t e, const char* what);
 
 // uint8 tensor map of the given rank: dims[0] innermost (elements = bytes),
 // strides[i] = byte stride of dimension i + 1, box per dimension, 64- or
-// 128-byte swizzle, zero fill out of bounds.  False when the driver rejects it.
+// 128-byte swizzle, zero fill out of bounds.  False when cuTensorMapEncodeTiled rejects it.
 bool encode_tma_u8(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
                    const uint32_t* box, int swizzle_bytes);
 // 2-D uint8 tensor map [rows][inner] (row pitch = inner bytes), box
