@@ -133,7 +133,7 @@ struct Smem {
   float fac[kNH];        // rescale factor of the current block; 1 / row sum at the end
   int mx[kNH];           // block maximum per head (order-preserving ints)
   unsigned long long bar_qraw, bar_q, bar_kv_full[NST], bar_kv_empty[NST][kRowQ];
-  unsigned long long bar_s_full, bar_s_free, bar_p_full, bar_pv_done;
+  unsigned long long bar_s_full, bar_s_free, bar_p_full[kRowQ], bar_pv_done;  // P published per key quarter
   unsigned long long bar_kv_split;         // blockwise rows: the block's hi / lo terms are written
   unsigned long long bar_kv_q[kRowQ];      // blockwise rows: key quarter q has landed (raw) with s_row
   uint32_t tmem_base;
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     }
     mbar_init(smem_u32(&s.bar_s_full), 1);
     mbar_init(smem_u32(&s.bar_s_free), kSoftThreads);
-    mbar_init(smem_u32(&s.bar_p_full), kSoftThreads);
+    for (int q = 0; q < kRowQ; ++q) mbar_init(smem_u32(&s.bar_p_full[q]), kSoftThreads / kRowQ);
     mbar_init(smem_u32(&s.bar_pv_done), 1);
     mbar_init(smem_u32(&s.bar_kv_split), kSoftThreads);
     for (int q = 0; q < kRowQ; ++q) mbar_init(smem_u32(&s.bar_kv_q[q]), kProdThreads);
@@ -590,6 +590,10 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
               tmem_st16(a, v);
             }
             tmem_wait_st();
+            // every lane quarter is rescaled before any quarter's P is
+            // published: each PV MMA of this block writes all 128 lanes
+            tc_fence_before();
+            named_bar_sync(1, kSoftThreads);
           }
         }
         // ---- P row r (this thread's 32 heads) and the row sums
@@ -614,21 +618,20 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
             *reinterpret_cast<uint4*>(p_hi + r * 64 + sw64(r, c4)) = quant16(x);
           }
         }
-        // PV of the previous block (possibly the previous item's last) must
-        // have completed: the single P-lo buffer is read by it, and P of this
-        // block is only published once that PV was issued (so p_full never
-        // runs a phase ahead of its consumer).
-        if (g > 0) {
-          wt = mbar_wait(smem_u32(&s.bar_pv_done), (g - 1) & 1, p.err);
-          if (!named_bar_and(1, kSoftThreads, wt)) { ok = false; break; }
-        }
+        // This warp's key quarter of the previous block's PV (possibly the
+        // previous item's last) must have completed: it reads this quarter's
+        // P-lo rows, and P is published per key quarter only once the quarter
+        // before it was consumed (so p_full[q] never runs a phase ahead).  No
+        // barrier here: one quarter's warps publish before another's, and PV
+        // starts on the first quarters.  A timeout is recorded, not taken.
+        if (g > 0) mbar_wait(smem_u32(&s.bar_kv_empty[(g - 1) % NST][warp & 3]), ((g - 1) / NST) & 1, p.err);
         if (PP == 2) {
 #pragma unroll
           for (int c = 0; c < 2; ++c) *reinterpret_cast<uint4*>(s.plo + r * 64 + sw64(r, half * 2 + c)) = lo_keep[c];
         }
         fence_proxy_async_smem();
-        tc_fence_before();  // this thread's TMEM reads (S; the epilogue's O) precede the PV it releases
-        mbar_arrive(smem_u32(&s.bar_p_full));
+        tc_fence_before();  // this thread's TMEM reads (S) precede the PV it releases
+        mbar_arrive(smem_u32(&s.bar_p_full[warp & 3]));
       }
       if (!ok) break;
       gb += nblk;
@@ -692,6 +695,9 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
           }
         }
       }
+      // The O^T reads precede the next item's first PV: every softmax thread
+      // passes that item's start barrier before any of them publishes P.
+      tc_fence_before();
       // linv (s.fac) is rewritten by the next item's slow path only after the
       // named barrier at that item's start; every thread has read it by then
       I = In;
@@ -769,10 +775,12 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     if (leader) s.q_issued = q_issued;
   } else if (warp == kPvWarp) {
     // =================================================================== PV issuer
-    // PV of block g once its P is written.  A warp of its own, so that PV is
-    // never queued behind the issue of the next QK.  An item's first PV
-    // overwrites O^T; its P is published only after the softmax warps have
-    // read the previous item's O^T.
+    // PV of block g, key quarter by key quarter as the softmax warps publish
+    // P per quarter.  A warp of its own, so that PV is never queued behind
+    // the issue of the next QK.  Every PV MMA writes all 128 O^T lanes: an
+    // item's first PV overwrites O^T, and the softmax publishes no P before
+    // all its warps have read the previous item's O^T (the item-start
+    // barrier) and, after a rescale, rescaled all lanes (a barrier).
     setmaxnreg_dec<kLowRegs>();
     const bool leader = elect_one();
     constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, kNH, 1, 1);
@@ -784,17 +792,21 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
       const Item I = item_at(p, w, groups);
       for (int j = 0; j < I.nblk; ++j) {
         const int g = gb + j;
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_p_full), g & 1, p.err))) { ok = false; break; }
-        tc_fence_after();  // after the softmax's TMEM reads and rescale of O^T
         // O^T[512 vcols x 64 heads] += V^T P^T over the block's 128 keys, one
-        // 32-key quarter at a time with the four 128-column tiles interleaved;
-        // each quarter's rows go back to the gather when its MMAs complete.
-        // P hi sits in the slot's rope chunk, P lo in its own buffer.
+        // 32-key quarter at a time (issued once that quarter's P is written)
+        // with the four 128-column tiles interleaved; each quarter's rows go
+        // back to the gather when its MMAs complete.  P hi sits in the slot's
+        // rope chunk, P lo in its own buffer.
         const int slot = g % NST;
         const uint64_t slot_off = static_cast<uint64_t>((slot * KVP * kKVBytes) >> 4);
-        if (leader) {
 #pragma unroll
-          for (int ks = 0; ks < kRowQ; ++ks) {
+        for (int ks = 0; ks < kRowQ; ++ks) {
+          if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_p_full[ks]), g & 1, p.err))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();  // after the softmax's TMEM reads and rescale of O^T
+          if (leader) {
 #pragma unroll
             for (int pp = 0; pp < PP; ++pp)
 #pragma unroll
@@ -810,8 +822,10 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
                 }
             mma_commit(smem_u32(&s.bar_kv_empty[slot][ks]));
           }
-          mma_commit(smem_u32(&s.bar_pv_done));
+          __syncwarp();
         }
+        if (!ok) break;
+        if (leader) mma_commit(smem_u32(&s.bar_pv_done));
         __syncwarp();
       }
       gb += I.nblk;
