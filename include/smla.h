@@ -109,9 +109,12 @@ smla_status_t smla_topk(const float* scores, int64_t score_stride, smla_seqs_t s
  *   indices      u32 [T, indices_stride] physical rows; topk_lengths u32 [T]
  *                (each <= indices_stride)
  *   out          bf16 [T, H, v_depth] (output)
- * Supported: H in {16, 64, 128} (any multiple of 64, or 16..64 padded),
- * v_depth == 512, scale_block_size in {0, 32} or >= 576; attn_sink must be
- * NULL (the pages do not define its semantics).
+ * Supported: H in {16, 32, 48, 64} or any multiple of 64; v_depth == 512;
+ * scale_block_size in {0, 32} or >= 576, where 32 (block scales) requires e4m3
+ * q; attn_sink must be NULL (the pages do not define its semantics).
+ * Alignment: q, latent_pool and out 16 bytes; indices, topk_lengths and
+ * scales 4 bytes.  Other shapes return SMLA_ERR_UNSUPPORTED, misaligned
+ * pointers SMLA_ERR_INVALID_ARG; nothing is launched then.
  * Runs on tcgen05 FP8 tensor cores with f32 TMEM accumulation: e4m3 q is
  * used natively; bf16 q and the softmax weights P (bf16-accuracy path) are
  * carried as two e4m3 terms (hi + lo) so that the products stay on the FP8
