@@ -97,13 +97,15 @@ __device__ __forceinline__ uint32_t phys_row(const Params& p, int b, int key) {
 }
 
 // Writes the physical row of logical key i to out[o] (page ids from the
-// shared-memory copy `ptab` when it holds the sequence's pages).
-__device__ __forceinline__ void emit(const Params& p, int b, const int* ptab, uint32_t* out, int o, int i) {
+// shared-memory copy `ptab` of the sequence's first nptab pages when it holds
+// key i's page).
+__device__ __forceinline__ void emit(const Params& p, int b, const int* ptab, int nptab, uint32_t* out, int o,
+                                     int i) {
   if (o >= p.k) {
     atomicOr(p.err, kErrShape);
     return;
   }
-  if (ptab) {
+  if (ptab && (i >> p.page_shift) < nptab) {
     const int pid = ptab[i >> p.page_shift];
     out[o] = pid >= 0 ? (static_cast<uint32_t>(pid) << p.page_shift) | static_cast<uint32_t>(i & (p.page_size - 1))
                       : phys_row(p, b, i);
@@ -178,7 +180,8 @@ __global__ void __launch_bounds__(kThreads, E4 <= 4 ? 3 : 1) topk_reg_kernel(con
   __shared__ uint32_t hist[kBins];
   __shared__ int warp_tot[kWarps + 1];
   __shared__ uint32_t s_wmin[kWarps], s_wmax[kWarps];
-  __shared__ int gt_w[E4][kWarps], eq_w[E4][kWarps];
+  __shared__ uint32_t cnt_w[E4][kWarps];  // per (e, warp): gt count | tie count << 16
+  __shared__ int ptab[256 * E4];          // page ids of the token's sequence (n / 8 pages at most)
   __shared__ int sh_b, sh_bin, sh_above, sh_cnt;
 
   const int t = blockIdx.x;
@@ -222,6 +225,9 @@ __global__ void __launch_bounds__(kThreads, E4 <= 4 ? 3 : 1) topk_reg_kernel(con
     }
   }
   auto valid = [&](int i) { return 4 * ((i >> 2) * kThreads + tid) + (i & 3) < n; };
+  // n <= 2048 * E4 and page_size >= 8, so the valid keys span at most 256 * E4 pages
+  const int npages = min(p.max_pages, (n + p.page_size - 1) >> p.page_shift);
+  for (int i = tid; i < npages; i += kThreads) ptab[i] = p.page_table[static_cast<int64_t>(b) * p.max_pages + i];
   kmin = __reduce_min_sync(0xffffffffu, kmin);
   kmax = __reduce_max_sync(0xffffffffu, kmax);
   if (lane == 0) {
@@ -265,81 +271,112 @@ __global__ void __launch_bounds__(kThreads, E4 <= 4 ? 3 : 1) topk_reg_kernel(con
       }
     }
   }
-  // ---- compaction in key order.  gt: above the candidates' prefix (or a
-  // whole-taken candidate); eq: a candidate tie, taken while fewer than krem
-  // ties precede it.
-  int g_cnt[E4], e_cnt[E4];
+  // ---- compaction in key order.  Per key two flags, taken once: gt (above
+  // the candidates' prefix, or a candidate of a bin taken whole) and tie (a
+  // candidate, taken while fewer than krem ties precede it).  Key 4e+j of
+  // this thread has its gt flag at bit j and its tie flag at bit 4+j of byte
+  // e&3 of fl[e>>2].
+  const uint32_t bin_max = hi_val | ~hi_mask;
+  uint32_t fl[(E4 + 3) / 4];
+#pragma unroll
+  for (int w = 0; w < (E4 + 3) / 4; ++w) fl[w] = 0u;
 #pragma unroll
   for (int e = 0; e < E4; ++e) {
-    int g = 0, q = 0;
+    uint32_t byte = 0u;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int i = 4 * e + j;
-      if (!valid(i)) continue;
-      const bool cand = (u[i] & hi_mask) == hi_val;
-      g += (u[i] > (hi_val | ~hi_mask) || (whole && cand)) ? 1 : 0;
-      q += (!whole && cand) ? 1 : 0;
+      const bool ok = valid(i);
+      const bool cand = ok && (u[i] & hi_mask) == hi_val;
+      const bool gt = (ok && u[i] > bin_max) || (whole && cand);
+      const bool tie = !whole && cand;
+      byte |= (gt ? 1u : 0u) << j;
+      byte |= (tie ? 1u : 0u) << (4 + j);
     }
-    // warp-exclusive prefix of g and q
-    int gi = g, qi = q;
+    fl[e >> 2] |= byte << (8 * (e & 3));
+  }
+  auto flags = [&](int e) { return (fl[e >> 2] >> (8 * (e & 3))) & 0xffu; };
+  // Lane prefix sums of the two counts, two e per 32-bit word: e's gt count
+  // in bits 16(e&1)..+7 and its tie count in the next 8 bits.  A warp holds
+  // at most 128 of either per e, so the 8-bit fields never carry.
+  constexpr int NW = (E4 + 1) / 2;
+  uint32_t lex[NW];
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    uint32_t c = 0u;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (2 * w + h >= E4) continue;
+      const uint32_t f = flags(2 * w + h);
+      c |= (static_cast<uint32_t>(__popc(f & 0xfu)) | (static_cast<uint32_t>(__popc(f >> 4)) << 8)) << (16 * h);
+    }
+    uint32_t x = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int a = __shfl_up_sync(0xffffffffu, gi, o), c = __shfl_up_sync(0xffffffffu, qi, o);
-      if (lane >= o) {
-        gi += a;
-        qi += c;
+      const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    lex[w] = x - c;
+    if (lane == 31) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (2 * w + h >= E4) continue;
+        const uint32_t tot = (x >> (16 * h)) & 0xffffu;
+        cnt_w[2 * w + h][warp] = (tot & 0xffu) | ((tot >> 8) << 16);  // gt | tie << 16
       }
     }
-    if (lane == 31) {
-      gt_w[e][warp] = gi;
-      eq_w[e][warp] = qi;
-    }
-    g_cnt[e] = gi - g;
-    e_cnt[e] = qi - q;
   }
   __syncthreads();
   if (warp == 0) {
-    // exclusive prefix over (e, warp) in key order: E4 * 16 entries, lane l takes entries l, l+32, ...
-    int run_g = 0, run_q = 0;
+    // exclusive prefix over (e, warp) in key order, both counts in one word
+    // (a row holds at most 2048 * E4 <= 16384 keys); lane l takes entries
+    // l, l + 32, ...
+    uint32_t run = 0u;
     for (int base = 0; base < E4 * kWarps; base += 32) {
       const int idx = base + lane;
-      const int g = idx < E4 * kWarps ? gt_w[idx / kWarps][idx % kWarps] : 0;
-      const int q = idx < E4 * kWarps ? eq_w[idx / kWarps][idx % kWarps] : 0;
-      int gi = g, qi = q;
+      const uint32_t v = idx < E4 * kWarps ? cnt_w[idx / kWarps][idx % kWarps] : 0u;
+      uint32_t x = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int a = __shfl_up_sync(0xffffffffu, gi, o), c = __shfl_up_sync(0xffffffffu, qi, o);
-        if (lane >= o) {
-          gi += a;
-          qi += c;
-        }
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
       }
       __syncwarp();
-      if (idx < E4 * kWarps) {
-        gt_w[idx / kWarps][idx % kWarps] = run_g + gi - g;
-        eq_w[idx / kWarps][idx % kWarps] = run_q + qi - q;
-      }
-      run_g += __shfl_sync(0xffffffffu, gi, 31);
-      run_q += __shfl_sync(0xffffffffu, qi, 31);
+      if (idx < E4 * kWarps) cnt_w[idx / kWarps][idx % kWarps] = run + x - v;
+      run += __shfl_sync(0xffffffffu, x, 31);
     }
   }
   __syncthreads();
+  // The emitted position of a taken key is the number of taken keys before
+  // it: the gt keys before it plus min(ties before it, krem).
 #pragma unroll
   for (int e = 0; e < E4; ++e) {
-    int gb = gt_w[e][warp] + g_cnt[e], qb = eq_w[e][warp] + e_cnt[e];
+    const uint32_t f = flags(e);
+    if (f == 0u) continue;
+    const uint32_t cw = cnt_w[e][warp];
+    const uint32_t lx = (lex[e >> 1] >> (16 * (e & 1))) & 0xffffu;
+    int gb = static_cast<int>((cw & 0xffffu) + (lx & 0xffu));
+    int qb = static_cast<int>((cw >> 16) + (lx >> 8));
+    const int key0 = 4 * (e * kThreads + tid);
+    const int pg = key0 >> p.page_shift;  // page_size >= 8: the four keys share a page
+    const int pid = pg < npages ? ptab[pg] : -1;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int i = 4 * e + j;
-      if (!valid(i)) continue;
-      const int key = 4 * (e * kThreads + tid) + j;
-      const bool cand = (u[i] & hi_mask) == hi_val;
-      if (u[i] > (hi_val | ~hi_mask) || (whole && cand)) {
-        emit(p, b, nullptr, out, gb + min(qb, krem), key);
-        ++gb;
-      } else if (!whole && cand) {
-        if (qb < krem) emit(p, b, nullptr, out, gb + qb, key);
-        ++qb;
+      const bool gt = (f >> j) & 1u, tie = (f >> (4 + j)) & 1u;
+      if (gt || (tie && qb < krem)) {
+        const int o = gb + min(qb, krem);
+        if (o >= k) {
+          atomicOr(p.err, kErrShape);
+        } else if (pid < 0) {
+          atomicOr(p.err, kErrPage);
+          out[o] = 0xFFFFFFFFu;
+        } else {
+          out[o] = (static_cast<uint32_t>(pid) << p.page_shift) |
+                   static_cast<uint32_t>((key0 + j) & (p.page_size - 1));
+        }
       }
+      gb += gt ? 1 : 0;
+      qb += tie ? 1 : 0;
     }
   }
   if (tid == 0) p.lens[t] = static_cast<uint32_t>(k);
@@ -515,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 3) topk_kernel(const Params p) {
         const uint32_t u = i < w1 ? key_at(i) : 0u;
         const bool sel = i < w1 && (u > bin_max || ((u & hi_mask) == hi_val && ((taken[i >> 5] >> (i & 31)) & 1u)));
         const uint32_t bsel = __ballot_sync(0xffffffffu, sel);
-        if (sel) emit(p, b, pt_cached ? ptab : nullptr, out, pos + __popc(bsel & lt), i);
+        if (sel) emit(p, b, pt_cached ? ptab : nullptr, npages, out, pos + __popc(bsel & lt), i);
         pos += __popc(bsel);
       }
       if (tid == 0) p.lens[t] = static_cast<uint32_t>(k);
@@ -580,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 3) topk_kernel(const Params p) {
     const int my_tie = tie + __popc(beq & lt);
     const bool sel = gt || (eq && my_tie < krem);
     const uint32_t bsel = __ballot_sync(0xffffffffu, sel);
-    if (sel) emit(p, b, pt_cached ? ptab : nullptr, out, pos + __popc(bsel & lt), i);
+    if (sel) emit(p, b, pt_cached ? ptab : nullptr, npages, out, pos + __popc(bsel & lt), i);
     pos += __popc(bsel);
     tie += __popc(beq);
   }
