@@ -252,14 +252,22 @@ __global__ void __launch_bounds__(kThreads, E4 <= 4 ? 3 : 1) topk_reg_kernel(con
     int top = 31 - __clz(diff);
     hi_mask = top == 31 ? 0u : ~((2u << top) - 1u);
     hi_val = kmax & hi_mask;
+    bool first = true;
     while (top >= 0) {
       const int sh = max(0, top - 10);
       const uint32_t dmask = (1u << (top - sh + 1)) - 1u;
       for (int i = tid; i < kBins; i += kThreads) hist[i] = 0;
       __syncthreads();
+      if (first) {  // every valid key lies between kmin and kmax, so it has their common prefix
 #pragma unroll
-      for (int i = 0; i < E; ++i)
-        if (valid(i) && (u[i] & hi_mask) == hi_val) atomicAdd(&hist[(u[i] >> sh) & dmask], 1u);
+        for (int i = 0; i < E; ++i)
+          if (valid(i)) atomicAdd(&hist[(u[i] >> sh) & dmask], 1u);
+        first = false;
+      } else {
+#pragma unroll
+        for (int i = 0; i < E; ++i)
+          if (valid(i) && (u[i] & hi_mask) == hi_val) atomicAdd(&hist[(u[i] >> sh) & dmask], 1u);
+      }
       __syncthreads();
       const int bin = select_bin(hist, krem, warp_tot, &sh_bin, &sh_above, &sh_cnt);
       hi_val |= static_cast<uint32_t>(bin) << sh;
