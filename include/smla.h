@@ -17,8 +17,9 @@
  * word.  Outputs of a call that recorded a device error are unspecified.
  *
  * Layouts are row-major and dense unless a stride is given.  "e4m3" is the
- * float8_e4m3fn byte format; "bf16" is bfloat16 bits.  Device pointers must
- * be 16-byte aligned.
+ * float8_e4m3fn byte format; "bf16" is bfloat16 bits.  Each call states the
+ * alignment its pointers need; a misaligned pointer returns
+ * SMLA_ERR_INVALID_ARG.
  */
 #ifndef SMLA_H_
 #define SMLA_H_
@@ -49,7 +50,8 @@ enum { SMLA_BF16 = 0, SMLA_E4M3 = 1 };
  * attend to logical keys 0..pos.  Logical key j of sequence b is physical
  * row page_table[b*max_pages + j/page_size]*page_size + j%page_size.
  * T = cu_q[B] (passed on the host so that no call reads device memory to
- * size its grid).  Requires q_len <= kv_len for every sequence. */
+ * size its grid).  Requires q_len <= kv_len for every sequence.  The three
+ * pointers must be 4-byte aligned. */
 typedef struct {
   const int32_t* cu_q;        /* [B+1] */
   const int32_t* kv_len;      /* [B] */
@@ -73,6 +75,7 @@ typedef struct {
  *   k_scale  f32  [phys_rows]       per physical row
  *   scores   f32  [T, score_stride] (output; score_stride >= max kv_len, multiple of 4)
  * H_idx must be 4, 8, 16, 32 or 64 (SMLA_ERR_UNSUPPORTED otherwise).
+ * Alignment: q, k_pool and scores 16 bytes; q_scale and k_scale 4 bytes.
  * The dot products run on tcgen05 FP8 tensor cores with f32 accumulation. */
 smla_status_t smla_indexer_scores(const uint8_t* q, const float* q_scale, const uint8_t* k_pool,
                                   const float* k_scale, int64_t phys_rows, smla_seqs_t seqs,
@@ -90,7 +93,8 @@ smla_status_t smla_indexer_scores(const uint8_t* q, const float* q_scale, const 
  *   indices[t, len..k) = 0xFFFFFFFF
  *   scores   f32 [T, score_stride] (entries past pos(t) are not read)
  *   indices  u32 [T, k] (output), topk_lengths u32 [T] (output)
- * 1 <= k <= 65536. NaN scores are unsupported (their order is unspecified). */
+ * 1 <= k <= 65536. NaN scores are unsupported (their order is unspecified).
+ * Alignment: scores 16 bytes; indices and topk_lengths 4 bytes. */
 smla_status_t smla_topk(const float* scores, int64_t score_stride, smla_seqs_t seqs, int32_t k,
                         uint32_t* indices, uint32_t* topk_lengths, cudaStream_t stream);
 
