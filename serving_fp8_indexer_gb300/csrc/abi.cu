@@ -199,6 +199,8 @@ smla_status_t smla_sparse_prefill(const void* q, int32_t q_dtype, const uint8_t*
   if (v_depth != 512) return fail(SMLA_ERR_UNSUPPORTED, "v_depth=%d: only 512 is supported", v_depth);
   if (!(scale_block_size == 0 || scale_block_size == 32 || scale_block_size >= 576))
     return fail(SMLA_ERR_UNSUPPORTED, "scale_block_size=%d: supported 0, 32 or >= 576", scale_block_size);
+  if (scale_block_size == 32 && q_dtype == SMLA_BF16)
+    return fail(SMLA_ERR_UNSUPPORTED, "scale_block_size=32 (block scales) requires e4m3 q");
   if (scale_block_size != 0 && !scales) return fail(SMLA_ERR_INVALID_ARG, "scales is NULL with scale_block_size != 0");
   if (attn_sink) return fail(SMLA_ERR_UNSUPPORTED, "attn_sink must be NULL");
   if (!(softmax_scale == softmax_scale) || softmax_scale > 3.0e38f || softmax_scale < -3.0e38f)

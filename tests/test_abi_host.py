@@ -52,6 +52,8 @@ def test_indexer_validation(lib):
     assert f(None, P, P, P, 64, _seqs(), 64, P, 64, None) == INVALID and "null" in _msg(lib)
     assert f(P + 8, P, P, P, 64, _seqs(), 64, P, 64, None) == INVALID and "aligned" in _msg(lib)
     assert f(P, P, P, P, 64, _seqs(null=True), 64, P, 64, None) == INVALID
+    bad = _lib.SeqsT(P + 2, P, P, 1, 1, 64, 4)   # seqs pointers need 4-byte alignment
+    assert f(P, P, P, P, 64, bad, 64, P, 64, None) == INVALID and "aligned" in _msg(lib)
     assert f(P, P, P, P, 0, _seqs(), 64, P, 64, None) == INVALID and "phys_rows" in _msg(lib)
     assert f(None, None, None, None, 0, _seqs(T=0), 64, None, 64, None) == 0   # empty batch: no-op
 
@@ -82,12 +84,15 @@ def test_prefill_validation(lib):
     assert call(H=24) == UNSUPPORTED and "H=" in _msg(lib)
     assert call(vd=256) == UNSUPPORTED and "v_depth" in _msg(lib)
     assert call(sbs=64) == UNSUPPORTED and "scale_block_size" in _msg(lib)
-    assert call(sbs=32) == INVALID and "scales" in _msg(lib)
+    assert call(sbs=32, qd=1) == INVALID and "scales" in _msg(lib)
+    assert call(sbs=32, sc=P) == UNSUPPORTED and "e4m3 q" in _msg(lib)   # block scales need e4m3 q
     assert call(sink=P) == UNSUPPORTED and "attn_sink" in _msg(lib)
     assert call(ss=float("nan")) == INVALID
     assert call(st=0) == INVALID
     assert call(out=None) == INVALID
     assert call(lat=P + 8) == INVALID
+    assert call(idx=P + 2) == INVALID and "aligned" in _msg(lib)
+    assert call(sc=P + 2, sbs=576) == INVALID and "aligned" in _msg(lib)
     assert call(T=0, q=None, lat=None, idx=None, ln=None, out=None) == 0
     assert call(T=-1) == INVALID
 
