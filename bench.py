@@ -21,7 +21,6 @@ import hashlib
 import json
 import math
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -75,21 +74,21 @@ def dtype_label(w):
     return "e4m3 MMA (bf16 q and P as e4m3 hi+lo), f32 accumulate"
 
 
-def profiled_traffic(kernel_src, profile_md, captured_tokens, tokens):
-    """DRAM bytes per launch from a committed ncu summary (read + write of a
-    smaller launch of the same kernel variant), scaled by the tokens a launch
-    processes.  None once the kernel source differs from the one captured."""
+def profiled_traffic(kernel_src, variant, tokens, caps_path=None):
+    """DRAM bytes per launch of `variant` from the committed ncu capture
+    (profiles/dram_traffic.json: dram__bytes_read.sum + dram__bytes_write.sum
+    of one launch at a size whose q and output exceed L2), scaled by the
+    tokens a launch processes (q, output and indices all scale with them).
+    None when there is no capture or the kernel source changed since."""
     try:
         src = open(os.path.join(ROOT, kernel_src), "rb").read()
-        md = open(os.path.join(ROOT, profile_md)).read()
-    except OSError:
+        caps = json.load(open(caps_path or os.path.join(ROOT, "profiles", "dram_traffic.json")))
+    except (OSError, ValueError):
         return None
-    if hashlib.sha1(src).hexdigest() not in md:
+    c = caps.get(variant)
+    if not c or c.get("source_sha1") != hashlib.sha1(src).hexdigest():
         return None
-    m = re.search(r"`dram__bytes_read.sum` / `dram__bytes_write.sum` \| ([0-9.]+) MB / ([0-9.]+) MB", md)
-    if not m:
-        return None
-    return (float(m.group(1)) + float(m.group(2))) * 1e6 * tokens / captured_tokens
+    return (float(c["dram_bytes_read"]) + float(c["dram_bytes_write"])) * tokens / float(c["tokens"])
 
 
 def peak_value(peaks, key):
@@ -275,139 +274,143 @@ def config_dict(w, world):
 
 
 # ----------------------------------------------------------------------------- our arm
-def run_ours(args, rank, world):
-    import numpy as np
-    import torch
+class Case:
+    """One workload resident on the device, and one step of the path over it
+    through the C ABI (indexer -> top-k -> attention, the stages it has)."""
 
-    from serving_fp8_indexer_gb300 import build as smla_build
-    smla_build.build()
-    import serving_fp8_indexer_gb300 as smla
-    from serving_fp8_indexer_gb300 import workloads as wl
+    def __init__(self, name, dev):
+        import numpy as np
+        import torch
 
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    w = make_workload(args.case)
-    s = w.seqs
-    T, H, k = s.T, w.H, w.topk
-    has_idx, has_attn = w.h_idx > 0, w.H > 0
-    stride = int(s.kv_len.max() + 3) // 4 * 4
-    pos = wl.token_positions(s)
-    kt = float((pos + 1).sum())
-
-    seqs = smla.Seqs.from_host(s, dev)
-    t_in = {}
-    if has_idx:
-        t_in["q_idx"] = torch.from_numpy(w.q_idx).to(dev)
-        t_in["q_scale"] = torch.from_numpy(w.q_scale).to(dev)
-        k_pool = torch.from_numpy(w.k_pool).to(dev)
-        k_scale = torch.from_numpy(w.k_scale).to(dev)
-        scores = torch.empty((T, stride), device=dev)
-        idx = torch.empty((T, k), dtype=torch.uint32, device=dev)
-        lens = torch.empty((T,), dtype=torch.uint32, device=dev)
-    else:
-        idx = torch.from_numpy(w.indices).to(dev)
-        lens = torch.from_numpy(w.topk_lengths).to(dev)
-    if has_attn:
-        latent = torch.from_numpy(w.latent).to(dev)
-        scales = None if w.scales is None else torch.from_numpy(w.scales).to(dev)
-        if w.q_dtype == wl.Q_BF16:
-            t_in["q_attn"] = torch.from_numpy(w.q_attn.view(np.int16)).view(torch.bfloat16).to(dev)
+        import serving_fp8_indexer_gb300 as smla
+        from serving_fp8_indexer_gb300 import workloads as wl
+        self.smla, self.torch = smla, torch
+        self.name = name
+        self.w = w = make_workload(name)
+        s = w.seqs
+        self.T, self.H, self.k = s.T, w.H, w.topk
+        self.has_idx, self.has_attn = w.h_idx > 0, w.H > 0
+        self.stride = int(s.kv_len.max() + 3) // 4 * 4
+        self.pos = wl.token_positions(s)
+        self.kt = float((self.pos + 1).sum())
+        self.dev = dev
+        self.seqs = smla.Seqs.from_host(s, dev)
+        self.t_in = {}
+        if self.has_idx:
+            self.t_in["q_idx"] = torch.from_numpy(w.q_idx).to(dev)
+            self.t_in["q_scale"] = torch.from_numpy(w.q_scale).to(dev)
+            self.k_pool = torch.from_numpy(w.k_pool).to(dev)
+            self.k_scale = torch.from_numpy(w.k_scale).to(dev)
+            self.scores = torch.empty((self.T, self.stride), device=dev)
+            self.idx = torch.empty((self.T, self.k), dtype=torch.uint32, device=dev)
+            self.lens = torch.empty((self.T,), dtype=torch.uint32, device=dev)
         else:
-            t_in["q_attn"] = torch.from_numpy(w.q_attn).to(dev)
-        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    n_kernels = (2 if has_idx else 0) + (1 if has_attn else 0)
+            self.idx = torch.from_numpy(w.indices).to(dev) if w.indices is not None else None
+            self.lens = torch.from_numpy(w.topk_lengths).to(dev) if w.topk_lengths is not None else None
+        if self.has_attn:
+            self.latent = torch.from_numpy(w.latent).to(dev)
+            self.scales = None if w.scales is None else torch.from_numpy(w.scales).to(dev)
+            if w.q_dtype == wl.Q_BF16:
+                self.t_in["q_attn"] = torch.from_numpy(w.q_attn.view(np.int16)).view(torch.bfloat16).to(dev)
+            else:
+                self.t_in["q_attn"] = torch.from_numpy(w.q_attn).to(dev)
+            self.out = torch.empty((self.T, self.H, 512), dtype=torch.bfloat16, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.n_kernels = (2 if self.has_idx else 0) + (1 if self.has_attn else 0)
+        attn_len = np.minimum(self.pos + 1, self.k) if self.has_idx else (
+            w.topk_lengths.astype(np.int64) if self.has_attn else np.zeros(0))
+        self.flops = sparse_flops(attn_len, self.H) if self.has_attn else 0.0
 
-    def step(ev=None, tin=None, o=None):
-        # tin / o: the step's input tensors and result (attention output, or
-        # the top-k indices for indexer-only workloads); default the bench's own
-        tin = t_in if tin is None else tin
-        o_idx = o if (o is not None and not has_attn) else idx
-        o_out = o if (o is not None and has_attn) else (out if has_attn else None)
+    def step(self, ev=None, tin=None, o=None):
+        """One pass of the path.  tin / o: the step's input tensors and result
+        (attention output, or the top-k indices for indexer-only workloads);
+        default the case's own.  ev: events recorded between the stages."""
+        smla, w = self.smla, self.w
+        tin = self.t_in if tin is None else tin
+        o_idx = o if (o is not None and not self.has_attn) else self.idx
+        o_out = o if (o is not None and self.has_attn) else (self.out if self.has_attn else None)
         if ev is not None:
-            ev[0].record(stream)
-        if has_idx:
-            smla.indexer_scores(tin["q_idx"], tin["q_scale"], k_pool, k_scale, seqs, scores)
+            ev[0].record(self.stream)
+        if self.has_idx:
+            smla.indexer_scores(tin["q_idx"], tin["q_scale"], self.k_pool, self.k_scale, self.seqs, self.scores)
             if ev is not None:
-                ev[1].record(stream)
-            smla.topk(scores, seqs, k, o_idx, lens)
+                ev[1].record(self.stream)
+            smla.topk(self.scores, self.seqs, self.k, o_idx, self.lens)
             if ev is not None:
-                ev[2].record(stream)
-        if has_attn:
-            smla.sparse_prefill(tin["q_attn"], latent, scales, w.scale_block_size, o_idx, lens, w.softmax_scale, o_out)
+                ev[2].record(self.stream)
+        if self.has_attn:
+            smla.sparse_prefill(tin["q_attn"], self.latent, self.scales, w.scale_block_size, o_idx, self.lens,
+                                w.softmax_scale, o_out)
             if ev is not None:
-                ev[3].record(stream)
+                ev[3].record(self.stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize(dev)
-    smla.check_device_errors()
-    attn_len = np.minimum(pos + 1, k) if has_idx else w.topk_lengths.astype(np.int64)
-    flops = sparse_flops(attn_len, H) if has_attn else 0.0
+    def time_steps(self, steps, warmup, graph=False, world=1, sampler=None):
+        """Device time of `steps` steps after `warmup`; returns (total ms,
+        per-stage mean ms)."""
+        torch = self.torch
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize(self.dev)
+        self.smla.check_device_errors()
+        g = None
+        if graph:
+            # launch-bound workloads: replay one step as a CUDA graph
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.step()
+            g.replay()
+            torch.cuda.synchronize(self.dev)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        if sampler is not None:
+            sampler.start()
+            time.sleep(0.3)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(self.dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for i in range(steps):
+            if g is not None:
+                g.replay()
+            else:
+                self.step(evs[i])
+        e1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        if world > 1:
+            torch.distributed.barrier()
+        clocks = sampler.stop() if sampler is not None else None
+        self.smla.check_device_errors()
+        total_ms = e0.elapsed_time(e1)
+        stage = {}
+        if g is None:
+            if self.has_idx:
+                stage["indexer"] = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+                stage["topk"] = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+            if self.has_attn:
+                a = 2 if self.has_idx else 0
+                stage["sparse_mla"] = statistics.mean(e[a].elapsed_time(e[3]) for e in evs)
+        return total_ms, stage, clocks
 
-    graph = None
-    if args.graph:
-        # launch-bound workloads: replay one step as a CUDA graph
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step()
-        graph.replay()
-        torch.cuda.synchronize(dev)
-
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", 0)))
-    sampler.start()
-    time.sleep(0.3)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        if graph is not None:
-            graph.replay()
-        else:
-            step(evs[i])
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        torch.distributed.barrier()
-    clocks = sampler.stop()
-    smla.check_device_errors()
-
-    total_ms = e0.elapsed_time(e1)
-    stage = {}
-    if graph is None:
-        if has_idx:
-            stage["indexer"] = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-            stage["topk"] = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-        if has_attn:
-            a = 2 if has_idx else 0
-            stage["sparse_mla"] = statistics.mean(e[a].elapsed_time(e[3]) for e in evs)
-    if world > 1:
-        keys = sorted(stage)
-        red = max_over_ranks([total_ms] + [stage[x] for x in keys], dev)
-        total_ms = red[0]
-        for i, x in enumerate(keys):
-            stage[x] = red[i + 1]
-    ms_step = total_ms / args.steps
-
-    # ---- end to end through the C ABI with host buffers (pinned), copies timed.
-    # Serving-style pipeline: every step copies its inputs in from pinned host
-    # memory and its result back out, on copy streams of their own, into two
-    # device buffer sets used in turn, so step i's copies overlap the compute
-    # of steps i - 1 and i + 1 (each step's copies stay inside the timed region).
-    e2e = None
-    if not args.no_e2e:
+    def e2e(self, steps, world):
+        """The same metric through the C ABI from pinned host buffers, host
+        copies inside the timed region.  Serving-style pipeline: every step
+        copies its inputs in and its result out on copy streams of their own,
+        into two device buffer sets used in turn, so step i's copies overlap
+        the compute of steps i - 1 and i + 1 (each step's copies stay inside
+        the timed region)."""
+        import numpy as np
+        torch, w = self.torch, self.w
+        from serving_fp8_indexer_gb300 import workloads as wl
         host = {name: (torch.from_numpy(w.q_attn.view(np.int16)).view(torch.bfloat16) if name == "q_attn" and
                        w.q_dtype == wl.Q_BF16 else
                        torch.from_numpy({"q_idx": w.q_idx, "q_scale": w.q_scale, "q_attn": w.q_attn}[name])).pin_memory()
-                for name in t_in}
-        res0 = out if has_attn else idx
-        h_out = (torch.empty((T, H, 512), dtype=torch.bfloat16) if has_attn else
-                 torch.empty((T, k), dtype=torch.int32)).pin_memory()
-        sets = [(t_in, res0), ({name: torch.empty_like(x) for name, x in t_in.items()}, torch.empty_like(res0))]
+                for name in self.t_in}
+        res0 = self.out if self.has_attn else self.idx
+        h_out = (torch.empty((self.T, self.H, 512), dtype=torch.bfloat16) if self.has_attn else
+                 torch.empty((self.T, self.k), dtype=torch.int32)).pin_memory()
+        sets = [(self.t_in, res0), ({name: torch.empty_like(x) for name, x in self.t_in.items()},
+                                    torch.empty_like(res0))]
+        dev, stream = self.dev, self.stream
         h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         in_ready = [torch.cuda.Event() for _ in range(2)]
         in_free = [torch.cuda.Event() for _ in range(2)]
@@ -416,7 +419,7 @@ def run_ours(args, rank, world):
         for b in range(2):  # all buffers start free
             in_free[b].record(stream)
             out_free[b].record(stream)
-        n_e2e = max(4, min(args.steps, 8))
+        n_e2e = max(4, min(steps, 8))
 
         def e2e_step(i):
             b = i % 2
@@ -428,12 +431,12 @@ def run_ours(args, rank, world):
                 in_ready[b].record(h2d)
             stream.wait_event(in_ready[b])
             stream.wait_event(out_free[b])
-            step(tin=tin, o=res)
+            self.step(tin=tin, o=res)
             in_free[b].record(stream)
             out_ready[b].record(stream)
             with torch.cuda.stream(d2h):
                 d2h.wait_event(out_ready[b])
-                h_out.copy_(res if has_attn else res.view(torch.int32), non_blocking=True)
+                h_out.copy_(res if self.has_attn else res.view(torch.int32), non_blocking=True)
                 out_free[b].record(d2h)
 
         for i in range(2):
@@ -452,38 +455,114 @@ def run_ours(args, rank, world):
         e2e_ms = a.elapsed_time(b_ev) / n_e2e
         if world > 1:
             e2e_ms = max_over_ranks([e2e_ms], dev)[0]
+        self.smla.check_device_errors()
         bi = sum(ht.numel() * ht.element_size() for ht in host.values())
         bo = h_out.numel() * h_out.element_size()
-        ev = weak_scaling_value(world, flops if has_attn else kt, e2e_ms)
-        e2e = {"value": ev / 1e12 if has_attn else ev, "unit": "TFLOP/s" if has_attn else "keys·tok/s",
-               "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo), "ms_per_step": e2e_ms}
+        ev = weak_scaling_value(world, self.flops if self.has_attn else self.kt, e2e_ms)
+        return {"value": ev / 1e12 if self.has_attn else ev, "unit": "TFLOP/s" if self.has_attn else "keys·tok/s",
+                "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo), "ms_per_step": e2e_ms}
 
+    def free(self):
+        for name in [n for n in vars(self) if isinstance(getattr(self, n), self.torch.Tensor)]:
+            setattr(self, name, None)
+        self.t_in = {}
+        self.torch.cuda.empty_cache()
+
+
+def attn_peaks(peaks, src, fp8_q, timed_s):
+    """(peak TFLOP/s of the attention's logical dtype, label): bf16 for bf16 q,
+    FP8 = 2 x the bf16 figure (the nominal ratio) for e4m3 q.  The burst bf16
+    figure applies to a timed region under a second, the sustained one to a
+    longer region."""
+    key = "bf16_tflops" if timed_s < 1.0 else "bf16_tflops_sustained"
+    bf16 = peak_value(peaks, key)
+    kind = "burst" if key == "bf16_tflops" else "sustained"
+    if fp8_q:
+        return 2.0 * bf16, f"{src} fp8 dense = 2 x bf16 ({kind})"
+    return bf16, f"{src} bf16 dense ({kind})"
+
+
+# Issued tcgen05 MMA work per unit of the method's FLOPs, by path: bf16 q and
+# the bf16-accuracy P each run as two e4m3 terms, and blockwise-scaled rows as
+# two e4m3 terms (hi + lo), so the FP8 pipe executes twice the logical
+# FLOPs on those paths (QK and PV alike); native e4m3 runs them once.
+def issued_ratio(w):
+    from serving_fp8_indexer_gb300 import workloads as wl
+    if w.q_dtype == wl.Q_BF16:
+        return 2.0
+    if 0 < w.scale_block_size < 576:
+        return 2.0
+    return 1.0
+
+
+def attn_variant(w):
+    from serving_fp8_indexer_gb300 import workloads as wl
+    q = "bf16 q" if w.q_dtype == wl.Q_BF16 else "e4m3 q"
+    sc = {0: "unit scale"}.get(w.scale_block_size, "tensorwise scale" if w.scale_block_size >= 576 else
+                               f"blockwise-{w.scale_block_size} scale")
+    return f"prefill_kernel, {q}, {sc}, H={w.H}"
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    from serving_fp8_indexer_gb300 import build as smla_build
+    smla_build.build()
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    c = Case(args.case, dev)
+    w = c.w
+    sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", 0)))
+    total_ms, stage, clocks = c.time_steps(args.steps, args.warmup, graph=args.graph, world=world, sampler=sampler)
+    if world > 1:
+        keys = sorted(stage)
+        red = max_over_ranks([total_ms] + [stage[x] for x in keys], dev)
+        total_ms = red[0]
+        for i, x in enumerate(keys):
+            stage[x] = red[i + 1]
+    ms_step = total_ms / args.steps
+    e2e = None if args.no_e2e else c.e2e(args.steps, world)
+    c_flops = c.flops
+
+    # the other attention workloads, kernel time only (same launch as the tests)
+    extra = {}
+    if not args.no_extra and args.case == "chunk":
+        c.free()
+        del c
+        for name in ("dsv32", "blockwise"):
+            x = Case(name, dev)
+            t, st, _ = x.time_steps(max(5, args.steps // 2), args.warmup)
+            extra[name] = (x.w, x.flops, st["sparse_mla"], t)
+            x.free()
+            del x
     if rank != 0:
         return
     peaks, src = load_peaks()
-    bf16_peak = peak_value(peaks, "bf16_tflops_sustained")
     hbm = peak_value(peaks, "hbm_gbs")
-    # the attention's tensor peak is that of the method's dtype: bf16 for bf16 q,
-    # FP8 (2 x the bf16 figure, the nominal ratio) for e4m3 q
-    fp8_q = w.q_dtype == wl.Q_E4M3
-    attn_peak = 2.0 * bf16_peak if fp8_q else bf16_peak
-    attn_peak_name = "fp8 dense = 2 x bf16 (sustained)" if fp8_q else "bf16 dense (sustained)"
+    fp8_q = w.q_dtype == 1
     stages = {}
     if "indexer" in stage:
-        idx_bytes = w.q_idx.nbytes + w.q_scale.nbytes + w.k_pool.nbytes + w.k_scale.nbytes + 4 * kt
-        stages["indexer"] = {"ms": stage["indexer"], "TFLOP/s": 1e-12 * kt * w.h_idx * 256 / (stage["indexer"] * 1e-3),
+        idx_bytes = w.q_idx.nbytes + w.q_scale.nbytes + w.k_pool.nbytes + w.k_scale.nbytes + 4 * c_kt(w)
+        fp8_peak = 2.0 * peak_value(peaks, "bf16_tflops")
+        tf_idx = 1e-12 * c_kt(w) * w.h_idx * 256 / (stage["indexer"] * 1e-3)
+        stages["indexer"] = {"ms": stage["indexer"], "TFLOP/s": tf_idx, "frac_fp8_peak": tf_idx / fp8_peak,
                              "GB/s_algorithmic": 1e-9 * idx_bytes / (stage["indexer"] * 1e-3)}
-        topk_bytes = 4 * kt + 4 * T * k + 4 * T
+        topk_bytes = 4 * c_kt(w) + 4 * w.seqs.T * w.topk + 4 * w.seqs.T
         gbs = 1e-9 * topk_bytes / (stage["topk"] * 1e-3)
         stages["topk"] = {"ms": stage["topk"], "GB/s_algorithmic": gbs, "frac_hbm": gbs / hbm}
+    flops = c_flops
     if "sparse_mla" in stage:
         tf = flops / (stage["sparse_mla"] * 1e-3) / 1e12
-        stages["sparse_mla"] = {"ms": stage["sparse_mla"], "TFLOP/s": tf, "frac_peak": tf / attn_peak,
+        peak, pname = attn_peaks(peaks, src, fp8_q, total_ms * 1e-3)
+        fp8_attn_peak = peak if fp8_q else 2.0 * peak
+        r = issued_ratio(w)
+        stages["sparse_mla"] = {"ms": stage["sparse_mla"], "TFLOP/s": tf, "frac_peak": tf / peak,
                                 "peak_dtype": "fp8" if fp8_q else "bf16"}
-    if has_attn:
+    if w.H:
         value, unit = weak_scaling_value(world, flops, ms_step) / 1e12, "TFLOP/s"
     else:
-        value, unit = weak_scaling_value(world, kt, ms_step), "keys·tok/s"
+        value, unit = weak_scaling_value(world, c_kt(w), ms_step), "keys·tok/s"
     line = {
         "metric": METRIC,
         "value": value,
@@ -499,37 +578,53 @@ def run_ours(args, rank, world):
         "data": "synthetic",
         "config": config_dict(w, world),
         "stages": stages,
-        "gpu_launches": n_kernels * args.steps,
+        "gpu_launches": (2 if w.h_idx else 0) * args.steps + (1 if w.H else 0) * args.steps,
         "clocks": clocks,
     }
     if args.graph:
         line["config"]["launch"] = "CUDA graph replay of one step"
-    if has_idx:
-        line["indexer_topk"] = {"value": world * kt / ((stage.get("indexer", ms_step) + stage.get("topk", 0.0)) * 1e-3),
+    if "indexer" in stage:
+        line["indexer_topk"] = {"value": world * c_kt(w) / ((stage["indexer"] + stage["topk"]) * 1e-3),
                                 "unit": "keys·tok/s"}
     if "sparse_mla" in stage:
         tf = stages["sparse_mla"]["TFLOP/s"]
-        # measured DRAM traffic, only for the variant the committed capture covers
-        # (128 heads, bf16 q, tensorwise scale: the end-to-end chunk's shapes)
-        traffic = None
-        if args.case in ("chunk", "chunk_small"):
-            traffic = profiled_traffic("serving_fp8_indexer_gb300/csrc/prefill.cu",
-                                       "profiles/prefill_kernel_chunk_small.md", 1024, int(w.seqs.T))
-        elif args.case in ("blockwise", "blockwise_small"):
-            traffic = profiled_traffic("serving_fp8_indexer_gb300/csrc/prefill.cu",
-                                       "profiles/prefill_kernel_blockwise_small.md", 3072, int(w.seqs.T))
+        traffic = profiled_traffic("serving_fp8_indexer_gb300/csrc/prefill.cu", attn_variant(w), int(w.seqs.T))
         line["roofline"] = {"bound": "tensor", "kernel": "prefill_kernel (sparse MLA)", "achieved": tf,
-                            "peak": attn_peak, "unit": "TFLOP/s", "frac": tf / attn_peak, "traffic": traffic,
-                            "peak_source": f"{src} {attn_peak_name}"}
+                            "peak": peak, "unit": "TFLOP/s", "frac": tf / peak, "traffic": traffic,
+                            "peak_source": pname,
+                            # the MMAs actually issued run on the FP8 pipe: their FLOPs
+                            # (r x the method's) against the FP8 peak
+                            "issued": {"mma": "tcgen05 kind::f8f6f4 (e4m3)", "flops_per_logical_flop": r,
+                                       "achieved": tf * r, "peak": fp8_attn_peak,
+                                       "frac": tf * r / fp8_attn_peak}}
     elif "topk" in stage:
         line["roofline"] = {"bound": "hbm", "kernel": "topk_kernel", "achieved": stages["topk"]["GB/s_algorithmic"],
                             "peak": hbm, "unit": "GB/s", "frac": stages["topk"]["frac_hbm"], "traffic": None,
                             "peak_source": f"{src} HBM copy"}
+    if extra:
+        line["other_workloads"] = {}
+        for name, (xw, xf, ms, t) in extra.items():
+            xfp8 = xw.q_dtype == 1
+            pk, pn = attn_peaks(peaks, src, xfp8, t * 1e-3)
+            tf = xf / (ms * 1e-3) / 1e12
+            line["other_workloads"][name] = {
+                "workload": xw.name, "stage": "sparse_mla", "ms": ms, "TFLOP/s": tf, "frac_peak": tf / pk,
+                "peak_source": pn, "issued_frac_fp8": tf * issued_ratio(xw) / (pk if xfp8 else 2.0 * pk),
+                "dtype": dtype_label(xw)}
     if e2e is not None:
         line["e2e"] = e2e
     if world == 1 and not args.no_cpu_baseline and args.case == "chunk":
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line), flush=True)
+
+
+def c_pos(w):
+    from serving_fp8_indexer_gb300 import workloads as wl
+    return wl.token_positions(w.seqs)
+
+
+def c_kt(w):
+    return float((c_pos(w) + 1).sum())
 
 
 def main():
@@ -542,9 +637,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", choices=sorted(CASES), default="chunk")
     ap.add_argument("--graph", action="store_true", help="replay each step as a CUDA graph")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other attention workloads")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.gpus != world:
+        sys.exit(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world}; launch N > 1 ranks with "
+                 f"torch.distributed.run --nproc-per-node {args.gpus}")
     if args.impl == "reference":
         run_reference(args, rank, world)
         return

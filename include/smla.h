@@ -83,9 +83,10 @@ smla_status_t smla_indexer_scores(const uint8_t* q, const float* q_scale, const 
                                   cudaStream_t stream);
 
 /* Stage 2 -- per-token top-k over the causally valid keys.
- * "sparse_index_fp8_sm100" (the score buffer "the top-k stage consumes",
- * verified by a top-k set match) and "mla_sm100_prefill_sparse_fp8"
- * (indices in physical-row space + per-query topk_lengths):
+ * "sparse_index_fp8_sm100" (the indexer's score buffer is this stage's
+ * input; the page verifies the result as a top-k set match) and
+ * "mla_sm100_prefill_sparse_fp8" (indices in physical-row space + per-query
+ * topk_lengths):
  *   topk_lengths[t] = min(k, pos(t)+1)
  *   indices[t, 0..len) = physical rows of the len largest scores[t, 0..pos(t)],
  *                        ties broken toward the lower logical key, emitted in
@@ -93,10 +94,18 @@ smla_status_t smla_indexer_scores(const uint8_t* q, const float* q_scale, const 
  *   indices[t, len..k) = 0xFFFFFFFF
  *   scores   f32 [T, score_stride] (entries past pos(t) are not read)
  *   indices  u32 [T, k] (output), topk_lengths u32 [T] (output)
+ * workspace: caller-owned device scratch of at least
+ * smla_topk_workspace_size(T, score_stride, k) bytes (16-byte aligned; may
+ * be NULL when that size is 0, which it is for every shape this build
+ * selects in one pass per row); its contents on entry do not matter and are
+ * unspecified on return.  A smaller workspace_bytes returns
+ * SMLA_ERR_INVALID_ARG.
  * 1 <= k <= 65536. NaN scores are unsupported (their order is unspecified).
  * Alignment: scores 16 bytes; indices and topk_lengths 4 bytes. */
+size_t smla_topk_workspace_size(int32_t T, int64_t score_stride, int32_t k);
 smla_status_t smla_topk(const float* scores, int64_t score_stride, smla_seqs_t seqs, int32_t k,
-                        uint32_t* indices, uint32_t* topk_lengths, cudaStream_t stream);
+                        uint32_t* indices, uint32_t* topk_lengths, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
 
 /* Stage 3 -- sparse MLA prefill attention.
  * "mla_sm100_prefill_sparse_fp8" (Modular Mojo function page: arguments,
@@ -134,6 +143,16 @@ smla_status_t smla_sparse_prefill(const void* q, int32_t q_dtype, const uint8_t*
  * word.  Returns SMLA_OK, SMLA_ERR_DEVICE_CHECK (out-of-range index or page
  * id), SMLA_ERR_TIMEOUT (a pipeline wait gave up) or SMLA_ERR_CUDA. */
 smla_status_t smla_check_device_errors(cudaStream_t stream);
+
+/* Self-test of the device timeout path: enqueues one kernel whose only
+ * thread waits, with a limit of limit_us microseconds (1 .. 1000000), on a
+ * pipeline barrier that nothing completes, exactly as the stage kernels
+ * wait on theirs.  When the limit passes, the kernel records the timeout
+ * in the device error word and returns, so the next
+ * smla_check_device_errors() reports SMLA_ERR_TIMEOUT.  No library function
+ * calls it; it exists so that the timeout path can be tested without a
+ * hung kernel. */
+smla_status_t smla_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream);
 
 /* Copies the calling thread's last error message (NUL-terminated, truncated
  * to n bytes) and returns its full length. */

@@ -10,9 +10,11 @@ from ._lib import (  # noqa: F401
     Seqs,
     SmlaError,
     indexer_scores,
+    topk_workspace_size,
     topk,
     sparse_prefill,
     check_device_errors,
+    selftest_wait_timeout,
     version,
     load,
 )

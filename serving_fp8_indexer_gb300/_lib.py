@@ -24,8 +24,8 @@ STATUS_NAMES = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTE
 SMLA_BF16 = 0
 SMLA_E4M3 = 1
 
-EXPORTED = ("smla_indexer_scores", "smla_topk", "smla_sparse_prefill", "smla_check_device_errors",
-            "smla_last_error", "smla_version")
+EXPORTED = ("smla_indexer_scores", "smla_topk_workspace_size", "smla_topk", "smla_sparse_prefill",
+            "smla_check_device_errors", "smla_selftest_wait_timeout", "smla_last_error", "smla_version")
 
 
 class SmlaError(RuntimeError):
@@ -57,13 +57,18 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib = ctypes.CDLL(p)
         vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
         lib.smla_indexer_scores.argtypes = [vp, vp, vp, vp, i64, SeqsT, i32, vp, i64, vp]
-        lib.smla_topk.argtypes = [vp, i64, SeqsT, i32, vp, vp, vp]
+        sz = ctypes.c_size_t
+        lib.smla_topk_workspace_size.argtypes = [i32, i64, i32]
+        lib.smla_topk_workspace_size.restype = sz
+        lib.smla_topk.argtypes = [vp, i64, SeqsT, i32, vp, vp, vp, sz, vp]
+        lib.smla_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
         lib.smla_sparse_prefill.argtypes = [vp, i32, vp, i64, vp, i32, vp, i32, vp, i32, i32, i32, f32, vp, vp, vp]
         lib.smla_check_device_errors.argtypes = [vp]
         lib.smla_last_error.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
         lib.smla_last_error.restype = ctypes.c_size_t
         lib.smla_version.restype = ctypes.c_char_p
-        for name in ("smla_indexer_scores", "smla_topk", "smla_sparse_prefill", "smla_check_device_errors"):
+        for name in ("smla_indexer_scores", "smla_topk", "smla_sparse_prefill", "smla_check_device_errors",
+                     "smla_selftest_wait_timeout"):
             getattr(lib, name).restype = ctypes.c_int
         if path is None:
             _lib = lib
@@ -142,13 +147,22 @@ def indexer_scores(q: torch.Tensor, q_scale: torch.Tensor, k_pool: torch.Tensor,
     return scores
 
 
+def topk_workspace_size(T: int, score_stride: int, k: int) -> int:
+    """Bytes of device scratch smla_topk needs for these sizes."""
+    return int(load().smla_topk_workspace_size(int(T), int(score_stride), int(k)))
+
+
 def topk(scores: torch.Tensor, seqs: Seqs, k: int, indices: torch.Tensor, topk_lengths: torch.Tensor,
-         stream=None):
-    """indices uint32 [T, k] physical rows (tail 0xFFFFFFFF), topk_lengths uint32 [T]."""
+         workspace: Optional[torch.Tensor] = None, stream=None):
+    """indices uint32 [T, k] physical rows (tail 0xFFFFFFFF), topk_lengths uint32 [T].
+    workspace: a uint8 CUDA tensor of at least topk_workspace_size() bytes,
+    or None when that size is 0."""
     lib = load()
+    ws = _ptr(workspace, torch.uint8, "workspace") if workspace is not None else None
+    wsb = int(workspace.numel()) if workspace is not None else 0
     st = lib.smla_topk(_ptr(scores, torch.float32, "scores", 2), int(scores.shape[1]), seqs.as_c(), int(k),
                        _ptr(indices, torch.uint32, "indices", 2), _ptr(topk_lengths, torch.uint32, "topk_lengths", 1),
-                       _stream(stream))
+                       ws, wsb, _stream(stream))
     _check(lib, st)
     return indices, topk_lengths
 
@@ -178,6 +192,12 @@ def sparse_prefill(q: torch.Tensor, latent: torch.Tensor, scales: Optional[torch
 def check_device_errors(stream=None):
     lib = load()
     _check(lib, lib.smla_check_device_errors(_stream(stream)))
+
+
+def selftest_wait_timeout(limit_us: int, stream=None):
+    """Enqueues the device timeout self-test (see smla_selftest_wait_timeout)."""
+    lib = load()
+    _check(lib, lib.smla_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def version() -> str:

@@ -108,6 +108,19 @@ int device_sm_count() {
   return g_sm_count[dev];
 }
 
+// One warp: lane 0 initialises an mbarrier expecting one arrival that never
+// comes and waits on its first phase with the given limit (the stage
+// kernels' bounded wait); the wait gives up, records kErrTimeout and the
+// kernel returns.
+__global__ void selftest_wait_kernel(unsigned* err, unsigned long long limit_ns) {
+  __shared__ __align__(8) unsigned long long bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    mbar_wait(smem_u32(&bar), 0, err, limit_ns);
+  }
+}
+
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 static bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -167,8 +180,17 @@ smla_status_t smla_indexer_scores(const uint8_t* q, const float* q_scale, const 
   return launch_indexer(q, q_scale, k_pool, k_scale, phys_rows, seqs, H_idx, scores, score_stride, err, stream);
 }
 
+size_t smla_topk_workspace_size(int32_t T, int64_t score_stride, int32_t k) {
+  (void)T;
+  (void)score_stride;
+  (void)k;
+  // Every supported row is selected by one CTA in one pass over its scores:
+  // no scratch beyond shared memory.
+  return 0;
+}
+
 smla_status_t smla_topk(const float* scores, int64_t score_stride, smla_seqs_t seqs, int32_t k, uint32_t* indices,
-                        uint32_t* topk_lengths, cudaStream_t stream) {
+                        uint32_t* topk_lengths, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   g_last_error.clear();
   smla_status_t st = check_seqs(seqs);
   if (st != SMLA_OK) return st;
@@ -176,6 +198,10 @@ smla_status_t smla_topk(const float* scores, int64_t score_stride, smla_seqs_t s
   if (score_stride < 4 || (score_stride & 3))
     return fail(SMLA_ERR_INVALID_ARG, "score_stride=%lld must be a positive multiple of 4",
                 static_cast<long long>(score_stride));
+  const size_t need = smla_topk_workspace_size(seqs.T, score_stride, k);
+  if (workspace_bytes < need || (need && !workspace))
+    return fail(SMLA_ERR_INVALID_ARG, "workspace: %zu bytes given, %zu needed", workspace_bytes, need);
+  if (workspace && !aligned16(workspace)) return fail(SMLA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   if (seqs.T == 0) return SMLA_OK;
   if (!scores || !indices || !topk_lengths) return fail(SMLA_ERR_INVALID_ARG, "null pointer");
   if (!aligned16(scores) || !aligned4(indices) || !aligned4(topk_lengths))
@@ -233,6 +259,19 @@ smla_status_t smla_check_device_errors(cudaStream_t stream) {
   if (e != cudaSuccess) return fail_cuda(e, "clear device error word");
   if (v & kErrTimeout) return fail(SMLA_ERR_TIMEOUT, "device error word 0x%x: a pipeline wait gave up", v);
   return fail(SMLA_ERR_DEVICE_CHECK, "device error word 0x%x: index/page/shape out of range", v);
+}
+
+smla_status_t smla_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream) {
+  g_last_error.clear();
+  if (limit_us < 1 || limit_us > 1000000)
+    return fail(SMLA_ERR_INVALID_ARG, "limit_us=%u must be in [1, 1000000]", limit_us);
+  unsigned* err = nullptr;
+  const smla_status_t st = device_err_ptr(&err);
+  if (st != SMLA_OK) return st;
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(err, static_cast<unsigned long long>(limit_us) * 1000ull);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail_cuda(e, "selftest launch");
+  return SMLA_OK;
 }
 
 }  // extern "C"

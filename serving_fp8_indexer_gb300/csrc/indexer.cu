@@ -71,6 +71,10 @@ struct __align__(1024) Smem {
   unsigned long long bar_q, bar_kfull[kStages], bar_kempty[kStages], bar_afull[2], bar_aempty[2], bar_drain;
   uint32_t tmem_base;
   int item_b, item_tt, item_kc;
+  // TMA loads issued by the producer and landings seen by the MMA issuer, so
+  // that a CTA whose wait gave up still waits (bounded) for the copies it has
+  // in flight before it exits
+  int k_issued, k_landed, q_landed;
 };
 
 template <int HIDX>
@@ -161,6 +165,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(&s.bar_drain), 1);
     fence_mbar_init();
+    s.k_issued = 0;
+    s.k_landed = 0;
+    s.q_landed = 0;
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&s.tmem_base), kTmemCols);
@@ -193,9 +200,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(smem_u32(&s.bar_q), kBN * kDepth);
       tma_load_2d(smem_u32(s.q), &tm_q, 0, t0 * HIDX, smem_u32(&s.bar_q));
       const int nbox = kBM / p.box_rows;
+      int issued = 0;
       for (int i = 0; i < n_tiles; ++i) {
         const int st = i % kStages;
         if (!mbar_wait(smem_u32(&s.bar_kempty[st]), ((i / kStages) & 1) ^ 1, p.err)) break;
+        ++issued;
         const int kt = kt_begin + i;
         int nload = 0;
         int rows[kBM / 8];
@@ -221,15 +230,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(smem_u32(s.k[st]) + bx * p.box_rows * kDepth, &tm_k, 0, rows[bx],
                         smem_u32(&s.bar_kfull[st]));
       }
+      s.k_issued = issued;
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && n_tiles > 0) {
       bool ok = mbar_wait(smem_u32(&s.bar_q), 0, p.err);
+      s.q_landed = ok ? 1 : 0;
       const uint32_t q_base = smem_u32(s.q);
+      int landed = 0;
       for (int i = 0; ok && i < n_tiles; ++i) {
         const int st = i % kStages, a = i & 1;
         if (!mbar_wait(smem_u32(&s.bar_kfull[st]), (i / kStages) & 1, p.err)) break;
+        landed = i + 1;
         if (!mbar_wait(smem_u32(&s.bar_aempty[a]), ((i >> 1) & 1) ^ 1, p.err)) break;
         tc_fence_after();
         const uint32_t k_base = smem_u32(s.k[st]);
@@ -242,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(smem_u32(&s.bar_kempty[st]));
         mma_commit(smem_u32(&s.bar_afull[a]));
       }
+      s.k_landed = landed;
       // Make sure no MMA is still writing TMEM when the CTA tears down.
       mma_commit(smem_u32(&s.bar_drain));
       mbar_wait(smem_u32(&s.bar_drain), 0, p.err);
@@ -320,6 +334,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // After a wait gave up: TMA loads still in flight land before the CTA
+  // exits (bounded waits; in the normal case every issued load has landed).
+  if (threadIdx.x == 0 && n_tiles > 0) {
+    if (!s.q_landed) mbar_wait(smem_u32(&s.bar_q), 0, p.err);
+    for (int i = s.k_landed; i < s.k_issued; ++i)
+      mbar_wait(smem_u32(&s.bar_kfull[i % kStages]), (i / kStages) & 1, p.err);
+  }
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 

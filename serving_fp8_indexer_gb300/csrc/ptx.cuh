@@ -59,14 +59,16 @@ SMLA_DEVICE_INLINE bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Waits for the phase with the given parity to complete.  Gives up after
-// kWaitLimitNs, records kErrTimeout and returns false.
-SMLA_DEVICE_INLINE bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err) {
+// limit_ns of %globaltimer (kWaitLimitNs by default), records kErrTimeout
+// and returns false.
+SMLA_DEVICE_INLINE bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* err,
+                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       atomicOr(err, kErrTimeout);
       return false;
     }

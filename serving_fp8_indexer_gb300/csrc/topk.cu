@@ -1,9 +1,10 @@
 // Stage 2: per-token top-k over the causally valid keys.
 //
-// The score buffer "the top-k stage consumes" ("sparse_index_fp8_sm100"
-// page) feeds per-query physical-row indices and topk_lengths
-// ("mla_sm100_prefill_sparse_fp8" page).  The pages do not describe the
-// selection algorithm; this one is a radix select:
+// Input: the indexer's score buffer ("sparse_index_fp8_sm100" page, module
+// summary); output: the per-query physical-row indices and topk_lengths the
+// sparse attention reads ("mla_sm100_prefill_sparse_fp8" page, arguments).
+// The pages do not describe the selection algorithm; this one is a radix
+// select:
 //   * one CTA per token; the token's valid scores (keys 0..pos) are read
 //     once from HBM (float4, coalesced) into shared memory as
 //     order-preserving 32-bit keys;

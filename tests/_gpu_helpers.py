@@ -103,6 +103,26 @@ def sample_tokens(seqs: wl.Seqs, per_seq: int, seed=0) -> np.ndarray:
     return np.array(out, dtype=np.int64)
 
 
+def stratified_tokens(seqs: wl.Seqs, per_seq: int = 512, seed=0) -> np.ndarray:
+    """Deterministic stratified sample of at least `per_seq` tokens of every
+    sequence (all of them when it has no more): its first and last token,
+    plus one token drawn uniformly from each of per_seq - 2 equal strata of
+    the positions in between, so every part of the sequence is covered."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for b in range(seqs.B):
+        a, e = int(seqs.cu_q[b]), int(seqs.cu_q[b + 1])
+        if e - a <= per_seq:
+            out += list(range(a, e))
+            continue
+        inner = np.arange(a + 1, e - 1)
+        strata = np.array_split(inner, per_seq - 2)
+        out += [a] + [int(rng.choice(st)) for st in strata] + [e - 1]
+    toks = np.array(out, dtype=np.int64)
+    assert len(np.unique(toks)) == len(toks)
+    return toks
+
+
 def q_attn_tensor(w: wl.Workload, dev="cuda"):
     if w.q_dtype == wl.Q_BF16:
         return torch.from_numpy(w.q_attn.view(np.int16)).view(torch.bfloat16).to(dev)

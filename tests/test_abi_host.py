@@ -61,12 +61,21 @@ def test_indexer_validation(lib):
 def test_topk_validation(lib):
     P = 0x10000
     f = lib.smla_topk
-    assert f(P, 64, _seqs(), 0, P, P, None) == UNSUPPORTED and "k=" in _msg(lib)
-    assert f(P, 64, _seqs(), 70000, P, P, None) == UNSUPPORTED
-    assert f(P, 62, _seqs(), 8, P, P, None) == INVALID
-    assert f(P, 64, _seqs(), 8, None, P, None) == INVALID
-    assert f(P + 4, 64, _seqs(), 8, P, P, None) == INVALID and "aligned" in _msg(lib)
-    assert f(None, 64, _seqs(T=0), 8, None, None, None) == 0
+    assert f(P, 64, _seqs(), 0, P, P, None, 0, None) == UNSUPPORTED and "k=" in _msg(lib)
+    assert f(P, 64, _seqs(), 70000, P, P, None, 0, None) == UNSUPPORTED
+    assert f(P, 62, _seqs(), 8, P, P, None, 0, None) == INVALID
+    assert f(P, 64, _seqs(), 8, None, P, None, 0, None) == INVALID
+    assert f(P + 4, 64, _seqs(), 8, P, P, None, 0, None) == INVALID and "aligned" in _msg(lib)
+    assert f(None, 64, _seqs(T=0), 8, None, None, None, 0, None) == 0
+    # workspace: the size query, and a misaligned workspace is refused
+    need = lib.smla_topk_workspace_size(16384, 8192, 2048)
+    assert need == 0
+    assert f(P, 64, _seqs(), 8, P, P, P + 8, 64, None) == INVALID and "workspace" in _msg(lib)
+
+
+def test_selftest_validation(lib):
+    assert lib.smla_selftest_wait_timeout(0, None) == INVALID and "limit_us" in _msg(lib)
+    assert lib.smla_selftest_wait_timeout(2000000, None) == INVALID
 
 
 def test_prefill_validation(lib):
@@ -98,7 +107,7 @@ def test_prefill_validation(lib):
 
 
 def test_last_error_truncates(lib):
-    lib.smla_topk(None, 64, _seqs(), 0, None, None, None)
+    lib.smla_topk(None, 64, _seqs(), 0, None, None, None, 0, None)
     full = lib.smla_last_error(None, 0)
     buf = ctypes.create_string_buffer(8)
     assert lib.smla_last_error(buf, 8) == full and len(buf.value) == 7

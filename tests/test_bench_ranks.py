@@ -54,15 +54,28 @@ def test_reference_arm_other_ranks_do_nothing():
     assert bench.run_reference(A(), 1, 2) is None
 
 
-def test_profiled_traffic_reads_the_committed_capture(tmp_path):
-    # the committed capture of the current kernel source parses to read + write
-    # bytes scaled by tokens; another source (sha1 mismatch) gives None
-    t = bench.profiled_traffic("serving_fp8_indexer_gb300/csrc/prefill.cu",
-                               "profiles/prefill_kernel_chunk_small.md", 1024, 16384)
-    assert t is not None and 3.0e9 < t < 5.0e9
-    md = tmp_path / "p.md"
-    md.write_text("sha1 0000\n| `dram__bytes_read.sum` / `dram__bytes_write.sum` | 1.0 MB / 2.0 MB |\n")
-    assert bench.profiled_traffic("serving_fp8_indexer_gb300/csrc/prefill.cu", str(md), 1, 2) is None
+def test_profiled_traffic_scales_a_capture_of_the_current_source(tmp_path):
+    # a capture of the current kernel source gives read + write bytes scaled
+    # by tokens; a capture of another source (sha1 mismatch) gives None
+    import hashlib
+    import json
+    src = "serving_fp8_indexer_gb300/csrc/prefill.cu"
+    sha = hashlib.sha1(open(os.path.join(bench.ROOT, src), "rb").read()).hexdigest()
+    cap = {"v": {"tokens": 4096, "dram_bytes_read": 1.0e9, "dram_bytes_write": 0.5e9, "source_sha1": sha},
+           "old": {"tokens": 4096, "dram_bytes_read": 1.0e9, "dram_bytes_write": 0.5e9, "source_sha1": "0" * 40}}
+    f = tmp_path / "caps.json"
+    f.write_text(json.dumps(cap))
+    assert bench.profiled_traffic(src, "v", 16384, str(f)) == pytest.approx(6.0e9)
+    assert bench.profiled_traffic(src, "old", 16384, str(f)) is None
+    assert bench.profiled_traffic(src, "missing", 16384, str(f)) is None
+
+
+def test_gpus_flag_must_match_world_size():
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--gpus", "2"], capture_output=True,
+                       text=True, env={**os.environ, "WORLD_SIZE": "1"})
+    assert r.returncode != 0 and "WORLD_SIZE" in r.stderr
 
 
 def test_dtype_labels_follow_the_workload():

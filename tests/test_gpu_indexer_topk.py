@@ -7,8 +7,7 @@ import torch
 import serving_fp8_indexer_gb300 as smla
 from serving_fp8_indexer_gb300 import workloads as wl
 
-from _gpu_helpers import (check_scores, check_topk_against, run_indexer, run_topk, sample_tokens,
-                          score_stride_for)
+from _gpu_helpers import check_scores, check_topk_against, run_indexer, run_topk
 
 pytestmark = pytest.mark.gpu
 
@@ -83,26 +82,6 @@ def test_empty_batch_is_noop():
     smla.topk(scores, seqs, 8, torch.empty((0, 8), dtype=torch.uint32, device="cuda"),
               torch.empty((0,), dtype=torch.uint32, device="cuda"))
     smla.check_device_errors()
-
-
-@pytest.mark.slow
-def test_e2e_chunk_indexer_topk_full_size_sampled():
-    """The end-to-end chunk at full size (8 x 8192 keys, 16384 tokens,
-    H_idx 64, top-2048), in the launch configuration the benchmark times;
-    sampled tokens against the oracle."""
-    w = wl.e2e_chunk()
-    seqs, scores = run_indexer(w)
-    toks = sample_tokens(w.seqs, 4)
-    rows = scores[torch.from_numpy(toks).cuda()].cpu().numpy()
-    ref, _ = check_scores(w, rows, toks, scores.shape[1])
-    idx, lens = run_topk(seqs, scores, w.topk, w.seqs.T)
-    gi = idx.view(torch.int32)[torch.from_numpy(toks).cuda()].cpu().numpy().view(np.uint32)
-    gl = lens.view(torch.int32)[torch.from_numpy(toks).cuda()].cpu().numpy().view(np.uint32)
-    check_topk_against(w, rows.astype(np.float64), gi, gl, toks, w.topk, exact=True)
-    check_topk_against(w, ref, gi, gl, toks, w.topk, exact=False)
-    # every token: the length rule and a filled tail
-    pos = wl.token_positions(w.seqs)
-    assert np.array_equal(lens.cpu().numpy(), np.minimum(pos + 1, w.topk).astype(np.uint32))
 
 
 @pytest.mark.parametrize("stride", [8192, 12288, 20000])

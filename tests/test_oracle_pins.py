@@ -339,3 +339,36 @@ def test_two_summation_orders_agree():
             z = math.fsum(e)
             ref = [math.fsum(e[j] * K[j, c] for j in range(n)) / z for c in range(0, 512, 37)]
             assert np.allclose(out[t, h, ::37], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_attention_e4m3_q_branch():
+    """The e4m3-q branch of the oracle, pinned two ways.  (1) Every finite
+    e4m3 value is exact in bf16, so the same q given as e4m3 bytes
+    (q_dtype 1) and as the bf16 bits of the same values (q_dtype 0) must
+    give identical results; a branch that decoded the bytes any other way
+    would not.  (2) k = every causal key against torch's float64
+    scaled_dot_product_attention with q taken from torch's float8 dtype."""
+    rng = np.random.default_rng(21)
+    latent, q8, idx = _attn_inputs(rng, 3, 5, 90, 40, q_dtype=1)
+    q16 = torch.from_numpy(q8).view(torch.float8_e4m3fn).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle.decode_bf16(q16), oracle.decode_e4m3(q8))
+    lens = np.array([40, 17, 1], np.uint32)
+    a = oracle.sparse_prefill(q8, 1, latent, None, 0, idx, lens, 0.07)
+    b = oracle.sparse_prefill(q16, 0, latent, None, 0, idx, lens, 0.07)
+    assert np.array_equal(a, b)
+    L, H, ps = 29, 3, 8
+    seqs = wl.make_seqs(rng, [L], [L], ps)
+    lat = wl.to_e4m3_bytes(rng.standard_normal((seqs.phys_rows, 576)).astype(np.float32))
+    q = wl.to_e4m3_bytes(rng.standard_normal((L, H, 576)).astype(np.float32))
+    rows = wl.logical_to_phys(seqs, 0, np.arange(L))
+    ind = np.full((L, L), 0xFFFFFFFF, np.uint32)
+    for t in range(L):
+        ind[t, :t + 1] = rows[:t + 1]
+    sc = 1 / math.sqrt(576)
+    out = oracle.sparse_prefill(q, 1, lat, None, 0, ind, np.arange(1, L + 1, dtype=np.uint32), sc)
+    K = torch.from_numpy(lat[rows]).view(torch.float8_e4m3fn).double()
+    Q = torch.from_numpy(q).view(torch.float8_e4m3fn).double().permute(1, 0, 2)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        Q[None], K[None, None].expand(1, H, L, 576), K[None, None, :, :512].expand(1, H, L, 512),
+        is_causal=True, scale=sc)[0].permute(1, 0, 2).numpy()
+    assert np.allclose(out, ref, rtol=1e-11, atol=1e-13)
