@@ -112,7 +112,8 @@ smla_status_t smla_topk(const float* scores, int64_t score_stride, smla_seqs_t s
  * scale_block_size modes) and "mla_prefill_sparse_qkv_fp8" (K and V share
  * the latent rows; V = the first v_depth columns).  For each token t and
  * head h, with n = topk_lengths[t] and K_j = dequant(latent_pool[indices[t,j]]):
- *   s_j = softmax_scale * q[t,h,:] . K_j,   p = softmax(s_0..s_{n-1}),
+ *   s_j = softmax_scale * q[t,h,:] . K_j,
+ *   p_j = exp(s_j) / (exp(sink_h) + sum_i exp(s_i))   (sink_h = attn_sink[h], or no term when NULL),
  *   out[t,h,:] = bf16_rne( sum_j p_j * K_j[0:v_depth] )     (zeros if n == 0)
  *   q            [T, H, 576], bf16 (q_dtype SMLA_BF16) or e4m3 (SMLA_E4M3)
  *   latent_pool  e4m3 [phys_rows, 576] (512 nope + 64 rope)
@@ -121,13 +122,16 @@ smla_status_t smla_topk(const float* scores, int64_t score_stride, smla_seqs_t s
  *                means one scale per row; 32 means 18 block scales per row
  *   indices      u32 [T, indices_stride] physical rows; topk_lengths u32 [T]
  *                (each <= indices_stride)
+ *   attn_sink    f32 [H] or NULL: one logit per head, in the units of the
+ *                scaled logits s_j, that joins every softmax denominator and
+ *                carries no value (the page names the argument without
+ *                defining it; this is the reading taken)
  *   out          bf16 [T, H, v_depth] (output)
  * Supported: H in {16, 32, 48, 64} or any multiple of 64; v_depth == 512;
  * scale_block_size in {0, 32} or >= 576, where 32 (block scales) requires e4m3
- * q; attn_sink must be NULL (the pages do not define its semantics).
- * Alignment: q, latent_pool and out 16 bytes; indices, topk_lengths and
- * scales 4 bytes.  Other shapes return SMLA_ERR_UNSUPPORTED, misaligned
- * pointers SMLA_ERR_INVALID_ARG; nothing is launched then.
+ * q.  Alignment: q, latent_pool and out 16 bytes; indices, topk_lengths,
+ * scales and attn_sink 4 bytes.  Other shapes return SMLA_ERR_UNSUPPORTED,
+ * misaligned pointers SMLA_ERR_INVALID_ARG; nothing is launched then.
  * Runs on tcgen05 FP8 tensor cores with f32 TMEM accumulation: e4m3 q is
  * used natively; bf16 q and the softmax weights P (bf16-accuracy path) are
  * carried as two e4m3 terms (hi + lo) so that the products stay on the FP8
@@ -138,6 +142,45 @@ smla_status_t smla_sparse_prefill(const void* q, int32_t q_dtype, const uint8_t*
                                   const uint32_t* topk_lengths, int32_t T, int32_t H,
                                   int32_t v_depth, float softmax_scale, const float* attn_sink,
                                   uint16_t* out, cudaStream_t stream);
+
+/* Dense causal MLA prefill over the paged latent cache, for prompts short
+ * enough that a top-k selection would keep every key.  "SM100MLA" (the
+ * dense MLA prefill struct page) and "mla_sm100_prefill_blockscale" (dense
+ * MLA prefill with a block-scaled FP8 cache): token t of sequence b attends
+ * to every logical key 0..pos(t) of b (pos as in smla_seqs_t), reached
+ * through the page table, so no indices are read:
+ *   out[t,h,:] = sum_{j <= pos(t)} p_j * K_j[0:v_depth],
+ *   K_j = dequant(latent_pool[phys(b, j)]), p and the sink as for
+ *   smla_sparse_prefill.
+ * This equals smla_sparse_prefill with indices[t] = phys(b, 0..pos(t)) and
+ * topk_lengths[t] = pos(t)+1.  T = seqs.T; q [T, H, 576] and out
+ * [T, H, 512] as there; the other arguments, supported shapes, alignment
+ * and errors as for smla_sparse_prefill. */
+smla_status_t smla_dense_prefill(const void* q, int32_t q_dtype, const uint8_t* latent_pool,
+                                 int64_t phys_rows, const float* scales, int32_t scale_block_size,
+                                 smla_seqs_t seqs, int32_t H, int32_t v_depth, float softmax_scale,
+                                 const float* attn_sink, uint16_t* out, cudaStream_t stream);
+
+/* Sparse MLA decode: the sparse attention of smla_sparse_prefill for few
+ * query tokens (one or two per sequence), the other serving phase of the
+ * same cache and indices ("mla_prefill_sparse_qkv_fp8", which names the
+ * FP8 decode QK / PV machinery the prefill reuses).  Same arguments, result
+ * and rules as smla_sparse_prefill.  When the (token, 64-head group) pairs
+ * are too few to fill the GPU, each token's key blocks are divided among
+ * several CTAs, whose partial outputs and log-sum-exps go to `workspace`
+ * and are merged by a second kernel.  workspace: caller-owned device
+ * scratch of at least smla_sparse_decode_workspace_size(T, H,
+ * indices_stride) bytes on the current device (16-byte aligned; NULL when
+ * that size is 0); contents on entry do not matter, unspecified on return;
+ * too small returns SMLA_ERR_INVALID_ARG. */
+size_t smla_sparse_decode_workspace_size(int32_t T, int32_t H, int32_t indices_stride);
+smla_status_t smla_sparse_decode(const void* q, int32_t q_dtype, const uint8_t* latent_pool,
+                                 int64_t phys_rows, const float* scales, int32_t scale_block_size,
+                                 const uint32_t* indices, int32_t indices_stride,
+                                 const uint32_t* topk_lengths, int32_t T, int32_t H,
+                                 int32_t v_depth, float softmax_scale, const float* attn_sink,
+                                 uint16_t* out, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
 
 /* Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns SMLA_OK, SMLA_ERR_DEVICE_CHECK (out-of-range index or page

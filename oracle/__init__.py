@@ -27,4 +27,5 @@ from .reference import (  # noqa: F401
     dequant_rows,
     softmax_weights,
     sparse_prefill,
+    dense_prefill,
 )

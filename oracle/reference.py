@@ -180,19 +180,37 @@ def dequant_rows(latent, scales, scale_block_size, rows, qk_depth=576):
     return x * sc[:, blk]
 
 
-def softmax_weights(s: np.ndarray) -> np.ndarray:
-    """Row softmax of a [H, n] logit matrix (max-subtracted, float64)."""
-    m = s.max(axis=1, keepdims=True)
+def softmax_weights(s: np.ndarray, sink=None) -> np.ndarray:
+    """Row softmax of a [H, n] logit matrix (max-subtracted, float64).  With
+    a per-head sink logit [H] (the attention sink argument of the
+    mla_sm100_prefill_sparse_fp8 page, which names it without defining it;
+    the reading taken: a logit that joins every denominator and carries no
+    value), p_j = exp(s_j) / (exp(sink_h) + sum_i exp(s_i)), so the row sums
+    to less than 1."""
+    if sink is None:
+        m = s.max(axis=1, keepdims=True)
+        e = np.exp(s - m)
+        return e / e.sum(axis=1, keepdims=True)
+    sk = np.asarray(sink, dtype=np.float64)[:, None]
+    m = np.maximum(s.max(axis=1, keepdims=True), sk)
     e = np.exp(s - m)
-    return e / e.sum(axis=1, keepdims=True)
+    return e / (e.sum(axis=1, keepdims=True) + np.exp(sk - m))
+
+
+def _attend(q_row, q_dtype, K, softmax_scale, v_depth, sink):
+    """One token's attention over the dequantised key rows K [n, 576]."""
+    q = decode_bf16(q_row) if q_dtype == 0 else decode_e4m3(q_row)  # [H, 576]
+    s = float(softmax_scale) * (q @ K.T)                              # [H, n]
+    return softmax_weights(s, sink) @ K[:, :v_depth]
 
 
 def sparse_prefill(q_attn, q_dtype, latent, scales, scale_block_size, indices, topk_lengths,
-                   softmax_scale, v_depth=512, tokens=None):
+                   softmax_scale, v_depth=512, tokens=None, attn_sink=None):
     """out[t, h, :] = sum_j p_j * V_j with s_j = softmax_scale * q[t,h] . K_j,
-    p = softmax(s) over j < topk_lengths[t], K_j = dequantised latent row
-    indices[t, j], V_j = K_j[:v_depth].  float64 [n, H, v_depth]; a token with
-    topk_lengths 0 yields zeros (reading: empty softmax contributes
+    p = softmax(s) over j < topk_lengths[t] (with the per-head sink logit
+    attn_sink[h] in the denominator when given), K_j = dequantised latent
+    row indices[t, j], V_j = K_j[:v_depth].  float64 [n, H, v_depth]; a token
+    with topk_lengths 0 yields zeros (reading: empty softmax contributes
     nothing).  ``q_dtype`` is 0 for bf16 bits, 1 for e4m3 bytes."""
     T, H, D = q_attn.shape
     tokens = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
@@ -203,8 +221,27 @@ def sparse_prefill(q_attn, q_dtype, latent, scales, scale_block_size, indices, t
             continue
         rows = np.asarray(indices[t, :n], dtype=np.int64)
         K = dequant_rows(latent, scales, scale_block_size, rows, D)   # [n, 576]
-        q = decode_bf16(q_attn[t]) if q_dtype == 0 else decode_e4m3(q_attn[t])  # [H, 576]
-        s = float(softmax_scale) * (q @ K.T)                          # [H, n]
-        p = softmax_weights(s)
-        out[i] = p @ K[:, :v_depth]
+        out[i] = _attend(q_attn[t], q_dtype, K, softmax_scale, v_depth, attn_sink)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Dense causal MLA prefill ("SM100MLA" struct page; "mla_sm100_prefill_
+# blockscale" for the block-scaled FP8 cache): every query token attends to
+# every cached key of its sequence up to its own position, read through the
+# page table; the latent dequantisation, softmax scale and sink are those of
+# the sparse prefill above.
+# ---------------------------------------------------------------------------
+def dense_prefill(q_attn, q_dtype, latent, scales, scale_block_size, cu_q, kv_len, page_table, page_size,
+                  softmax_scale, v_depth=512, tokens=None, attn_sink=None):
+    """out[t, h, :] over the logical keys 0..pos(t) of t's sequence,
+    float64 [n, H, v_depth]."""
+    pos, seq = token_positions(cu_q, kv_len)
+    T, H, D = q_attn.shape
+    tokens = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    out = np.zeros((len(tokens), H, v_depth), dtype=np.float64)
+    for i, t in enumerate(tokens):
+        rows = phys_rows_of(page_table, page_size, int(seq[t]), np.arange(int(pos[t]) + 1))
+        K = dequant_rows(latent, scales, scale_block_size, rows, D)
+        out[i] = _attend(q_attn[t], q_dtype, K, softmax_scale, v_depth, attn_sink)
     return out

@@ -13,6 +13,9 @@ from ._lib import (  # noqa: F401
     topk_workspace_size,
     topk,
     sparse_prefill,
+    dense_prefill,
+    sparse_decode_workspace_size,
+    sparse_decode,
     check_device_errors,
     selftest_wait_timeout,
     version,

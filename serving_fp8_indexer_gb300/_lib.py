@@ -25,6 +25,7 @@ SMLA_BF16 = 0
 SMLA_E4M3 = 1
 
 EXPORTED = ("smla_indexer_scores", "smla_topk_workspace_size", "smla_topk", "smla_sparse_prefill",
+            "smla_dense_prefill", "smla_sparse_decode_workspace_size", "smla_sparse_decode",
             "smla_check_device_errors", "smla_selftest_wait_timeout", "smla_last_error", "smla_version")
 
 
@@ -62,13 +63,18 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.smla_topk_workspace_size.restype = sz
         lib.smla_topk.argtypes = [vp, i64, SeqsT, i32, vp, vp, vp, sz, vp]
         lib.smla_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
+        lib.smla_dense_prefill.argtypes = [vp, i32, vp, i64, vp, i32, SeqsT, i32, i32, f32, vp, vp, vp]
+        lib.smla_sparse_decode_workspace_size.argtypes = [i32, i32, i32]
+        lib.smla_sparse_decode_workspace_size.restype = sz
+        lib.smla_sparse_decode.argtypes = [vp, i32, vp, i64, vp, i32, vp, i32, vp, i32, i32, i32, f32, vp, vp, vp,
+                                           sz, vp]
         lib.smla_sparse_prefill.argtypes = [vp, i32, vp, i64, vp, i32, vp, i32, vp, i32, i32, i32, f32, vp, vp, vp]
         lib.smla_check_device_errors.argtypes = [vp]
         lib.smla_last_error.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
         lib.smla_last_error.restype = ctypes.c_size_t
         lib.smla_version.restype = ctypes.c_char_p
-        for name in ("smla_indexer_scores", "smla_topk", "smla_sparse_prefill", "smla_check_device_errors",
-                     "smla_selftest_wait_timeout"):
+        for name in ("smla_indexer_scores", "smla_topk", "smla_sparse_prefill", "smla_dense_prefill",
+                     "smla_sparse_decode", "smla_check_device_errors", "smla_selftest_wait_timeout"):
             getattr(lib, name).restype = ctypes.c_int
         if path is None:
             _lib = lib
@@ -167,24 +173,73 @@ def topk(scores: torch.Tensor, seqs: Seqs, k: int, indices: torch.Tensor, topk_l
     return indices, topk_lengths
 
 
+def _q_arg(q: torch.Tensor):
+    if q.dtype == torch.bfloat16:
+        return SMLA_BF16, _ptr(q, torch.bfloat16, "q", 3)
+    return SMLA_E4M3, _ptr(q, torch.uint8, "q", 3)
+
+
 def sparse_prefill(q: torch.Tensor, latent: torch.Tensor, scales: Optional[torch.Tensor], scale_block_size: int,
                    indices: torch.Tensor, topk_lengths: torch.Tensor, softmax_scale: float, out: torch.Tensor,
-                   stream=None) -> torch.Tensor:
+                   attn_sink: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """out bf16 [T, H, 512] = sparse MLA prefill.  q is bf16 or uint8 (e4m3
     bytes) [T, H, 576]; latent uint8 e4m3 [phys_rows, 576]; scales f32
     [phys_rows, ceil(576/sbs)] or None; indices uint32 [T, stride];
-    topk_lengths uint32 [T]."""
+    topk_lengths uint32 [T]; attn_sink f32 [H] or None."""
     lib = load()
-    if q.dtype == torch.bfloat16:
-        qd, qp = SMLA_BF16, _ptr(q, torch.bfloat16, "q", 3)
-    else:
-        qd, qp = SMLA_E4M3, _ptr(q, torch.uint8, "q", 3)
+    qd, qp = _q_arg(q)
     T, H = int(q.shape[0]), int(q.shape[1])
     st = lib.smla_sparse_prefill(qp, qd, _ptr(latent, torch.uint8, "latent", 2), int(latent.shape[0]),
                                  _ptr(scales, torch.float32, "scales", 2), int(scale_block_size),
                                  _ptr(indices, torch.uint32, "indices", 2), int(indices.shape[1]),
                                  _ptr(topk_lengths, torch.uint32, "topk_lengths", 1), T, H, int(out.shape[2]),
-                                 float(softmax_scale), None, _ptr(out, torch.bfloat16, "out", 3), _stream(stream))
+                                 float(softmax_scale), _ptr(attn_sink, torch.float32, "attn_sink", 1),
+                                 _ptr(out, torch.bfloat16, "out", 3), _stream(stream))
+    _check(lib, st)
+    return out
+
+
+def dense_prefill(q: torch.Tensor, latent: torch.Tensor, scales: Optional[torch.Tensor], scale_block_size: int,
+                  seqs: Seqs, softmax_scale: float, out: torch.Tensor, attn_sink: Optional[torch.Tensor] = None,
+                  stream=None) -> torch.Tensor:
+    """out bf16 [T, H, 512] = dense causal MLA prefill: every token attends to
+    every key 0..pos of its sequence through the page table."""
+    lib = load()
+    qd, qp = _q_arg(q)
+    if int(q.shape[0]) != seqs.T:
+        raise ValueError("q.shape[0] != seqs.T")
+    st = lib.smla_dense_prefill(qp, qd, _ptr(latent, torch.uint8, "latent", 2), int(latent.shape[0]),
+                                _ptr(scales, torch.float32, "scales", 2), int(scale_block_size), seqs.as_c(),
+                                int(q.shape[1]), int(out.shape[2]), float(softmax_scale),
+                                _ptr(attn_sink, torch.float32, "attn_sink", 1), _ptr(out, torch.bfloat16, "out", 3),
+                                _stream(stream))
+    _check(lib, st)
+    return out
+
+
+def sparse_decode_workspace_size(T: int, H: int, indices_stride: int) -> int:
+    """Bytes of device scratch smla_sparse_decode needs on the current device."""
+    return int(load().smla_sparse_decode_workspace_size(int(T), int(H), int(indices_stride)))
+
+
+def sparse_decode(q: torch.Tensor, latent: torch.Tensor, scales: Optional[torch.Tensor], scale_block_size: int,
+                  indices: torch.Tensor, topk_lengths: torch.Tensor, softmax_scale: float, out: torch.Tensor,
+                  workspace: Optional[torch.Tensor], attn_sink: Optional[torch.Tensor] = None,
+                  stream=None) -> torch.Tensor:
+    """Sparse MLA decode (split-K over each token's keys); the arguments of
+    sparse_prefill plus a uint8 CUDA workspace of at least
+    sparse_decode_workspace_size() bytes (None when that is 0)."""
+    lib = load()
+    qd, qp = _q_arg(q)
+    T, H = int(q.shape[0]), int(q.shape[1])
+    ws = _ptr(workspace, torch.uint8, "workspace") if workspace is not None else None
+    wsb = int(workspace.numel()) if workspace is not None else 0
+    st = lib.smla_sparse_decode(qp, qd, _ptr(latent, torch.uint8, "latent", 2), int(latent.shape[0]),
+                                _ptr(scales, torch.float32, "scales", 2), int(scale_block_size),
+                                _ptr(indices, torch.uint32, "indices", 2), int(indices.shape[1]),
+                                _ptr(topk_lengths, torch.uint32, "topk_lengths", 1), T, H, int(out.shape[2]),
+                                float(softmax_scale), _ptr(attn_sink, torch.float32, "attn_sink", 1),
+                                _ptr(out, torch.bfloat16, "out", 3), ws, wsb, _stream(stream))
     _check(lib, st)
     return out
 

@@ -212,12 +212,15 @@ smla_status_t smla_topk(const float* scores, int64_t score_stride, smla_seqs_t s
   return launch_topk(scores, score_stride, seqs, k, indices, topk_lengths, err, stream);
 }
 
-smla_status_t smla_sparse_prefill(const void* q, int32_t q_dtype, const uint8_t* latent_pool, int64_t phys_rows,
-                                  const float* scales, int32_t scale_block_size, const uint32_t* indices,
-                                  int32_t indices_stride, const uint32_t* topk_lengths, int32_t T, int32_t H,
-                                  int32_t v_depth, float softmax_scale, const float* attn_sink, uint16_t* out,
-                                  cudaStream_t stream) {
-  g_last_error.clear();
+}  // extern "C"
+
+namespace smla {
+// Host-side checks shared by the attention entry points; T is the number of
+// query tokens, `keyed` says whether indices / topk_lengths are used.
+static smla_status_t check_attn(const void* q, int32_t q_dtype, const void* latent_pool, int64_t phys_rows,
+                                const float* scales, int32_t scale_block_size, bool keyed, const uint32_t* indices,
+                                int32_t indices_stride, const uint32_t* topk_lengths, int32_t T, int32_t H,
+                                int32_t v_depth, float softmax_scale, const float* attn_sink, const void* out) {
   if (T < 0) return fail(SMLA_ERR_INVALID_ARG, "T=%d must be >= 0", T);
   if (q_dtype != SMLA_BF16 && q_dtype != SMLA_E4M3) return fail(SMLA_ERR_INVALID_ARG, "q_dtype=%d", q_dtype);
   if (!(H >= 1 && ((H <= 64 && H % 16 == 0) || H % 64 == 0)))
@@ -228,22 +231,94 @@ smla_status_t smla_sparse_prefill(const void* q, int32_t q_dtype, const uint8_t*
   if (scale_block_size == 32 && q_dtype == SMLA_BF16)
     return fail(SMLA_ERR_UNSUPPORTED, "scale_block_size=32 (block scales) requires e4m3 q");
   if (scale_block_size != 0 && !scales) return fail(SMLA_ERR_INVALID_ARG, "scales is NULL with scale_block_size != 0");
-  if (attn_sink) return fail(SMLA_ERR_UNSUPPORTED, "attn_sink must be NULL");
   if (!(softmax_scale == softmax_scale) || softmax_scale > 3.0e38f || softmax_scale < -3.0e38f)
     return fail(SMLA_ERR_INVALID_ARG, "softmax_scale must be finite");
-  if (indices_stride < 1) return fail(SMLA_ERR_INVALID_ARG, "indices_stride must be >= 1");
+  if (keyed && indices_stride < 1) return fail(SMLA_ERR_INVALID_ARG, "indices_stride must be >= 1");
   if (T == 0) return SMLA_OK;
-  if (!q || !latent_pool || !indices || !topk_lengths || !out) return fail(SMLA_ERR_INVALID_ARG, "null pointer");
-  if (!aligned16(q) || !aligned16(latent_pool) || !aligned16(out) || !aligned4(indices) || !aligned4(topk_lengths) ||
-      (scales && !aligned4(scales)))
-    return fail(SMLA_ERR_INVALID_ARG, "q, latent_pool, out must be 16-byte aligned; indices/scales 4-byte aligned");
+  if (!q || !latent_pool || !out || (keyed && (!indices || !topk_lengths)))
+    return fail(SMLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(q) || !aligned16(latent_pool) || !aligned16(out) ||
+      (keyed && (!aligned4(indices) || !aligned4(topk_lengths))) || (scales && !aligned4(scales)) ||
+      (attn_sink && !aligned4(attn_sink)))
+    return fail(SMLA_ERR_INVALID_ARG,
+                "q, latent_pool, out must be 16-byte aligned; indices, scales and attn_sink 4-byte aligned");
   if (phys_rows < 1 || phys_rows >= (int64_t(1) << 31))
     return fail(SMLA_ERR_INVALID_ARG, "phys_rows=%lld out of range", static_cast<long long>(phys_rows));
+  if (static_cast<int64_t>(T) * H >= (int64_t(1) << 31)) return fail(SMLA_ERR_UNSUPPORTED, "T*H too large");
+  return SMLA_OK;
+}
+}  // namespace smla
+
+extern "C" {
+
+smla_status_t smla_sparse_prefill(const void* q, int32_t q_dtype, const uint8_t* latent_pool, int64_t phys_rows,
+                                  const float* scales, int32_t scale_block_size, const uint32_t* indices,
+                                  int32_t indices_stride, const uint32_t* topk_lengths, int32_t T, int32_t H,
+                                  int32_t v_depth, float softmax_scale, const float* attn_sink, uint16_t* out,
+                                  cudaStream_t stream) {
+  g_last_error.clear();
+  smla_status_t st = check_attn(q, q_dtype, latent_pool, phys_rows, scales, scale_block_size, true, indices,
+                                indices_stride, topk_lengths, T, H, v_depth, softmax_scale, attn_sink, out);
+  if (st != SMLA_OK || T == 0) return st;
   unsigned* err = nullptr;
-  smla_status_t st = device_err_ptr(&err);
+  st = device_err_ptr(&err);
   if (st != SMLA_OK) return st;
-  return launch_sparse_prefill(q, q_dtype, latent_pool, phys_rows, scales, scale_block_size, indices,
-                               indices_stride, topk_lengths, T, H, softmax_scale, out, err, stream);
+  AttnArgs a{q, q_dtype, latent_pool, phys_rows, scales, scale_block_size, indices, indices_stride, topk_lengths,
+             nullptr, T, H, softmax_scale, attn_sink, out, 1, nullptr, nullptr};
+  return launch_attention(a, err, stream);
+}
+
+smla_status_t smla_dense_prefill(const void* q, int32_t q_dtype, const uint8_t* latent_pool, int64_t phys_rows,
+                                 const float* scales, int32_t scale_block_size, smla_seqs_t seqs, int32_t H,
+                                 int32_t v_depth, float softmax_scale, const float* attn_sink, uint16_t* out,
+                                 cudaStream_t stream) {
+  g_last_error.clear();
+  smla_status_t st = check_seqs(seqs);
+  if (st != SMLA_OK) return st;
+  st = check_attn(q, q_dtype, latent_pool, phys_rows, scales, scale_block_size, false, nullptr, 0, nullptr, seqs.T,
+                  H, v_depth, softmax_scale, attn_sink, out);
+  if (st != SMLA_OK || seqs.T == 0) return st;
+  unsigned* err = nullptr;
+  st = device_err_ptr(&err);
+  if (st != SMLA_OK) return st;
+  AttnArgs a{q, q_dtype, latent_pool, phys_rows, scales, scale_block_size, nullptr, 0, nullptr,
+             &seqs, seqs.T, H, softmax_scale, attn_sink, out, 1, nullptr, nullptr};
+  return launch_attention(a, err, stream);
+}
+
+size_t smla_sparse_decode_workspace_size(int32_t T, int32_t H, int32_t indices_stride) {
+  if (T <= 0 || H <= 0 || indices_stride <= 0) return 0;
+  return decode_workspace_bytes(T, H, decode_splits(T, H, indices_stride));
+}
+
+smla_status_t smla_sparse_decode(const void* q, int32_t q_dtype, const uint8_t* latent_pool, int64_t phys_rows,
+                                 const float* scales, int32_t scale_block_size, const uint32_t* indices,
+                                 int32_t indices_stride, const uint32_t* topk_lengths, int32_t T, int32_t H,
+                                 int32_t v_depth, float softmax_scale, const float* attn_sink, uint16_t* out,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  g_last_error.clear();
+  smla_status_t st = check_attn(q, q_dtype, latent_pool, phys_rows, scales, scale_block_size, true, indices,
+                                indices_stride, topk_lengths, T, H, v_depth, softmax_scale, attn_sink, out);
+  if (st != SMLA_OK) return st;
+  const int nsplit = T > 0 ? decode_splits(T, H, indices_stride) : 1;
+  const size_t need = decode_workspace_bytes(T, H, nsplit);
+  if (workspace_bytes < need || (need && !workspace))
+    return fail(SMLA_ERR_INVALID_ARG, "workspace: %zu bytes given, %zu needed", workspace_bytes, need);
+  if (workspace && !aligned16(workspace)) return fail(SMLA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  if (T == 0) return SMLA_OK;
+  unsigned* err = nullptr;
+  st = device_err_ptr(&err);
+  if (st != SMLA_OK) return st;
+  // workspace: partial outputs [T, nsplit, H, 512] f32, then (at the next
+  // 256-byte boundary) log2-sum-exps [T, nsplit, H] f32
+  float* part_o = static_cast<float*>(workspace);
+  const size_t o_bytes = (static_cast<size_t>(T) * nsplit * H * 512 * sizeof(float) + 255) & ~size_t(255);
+  float* part_lse = nsplit > 1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes) : nullptr;
+  AttnArgs a{q, q_dtype, latent_pool, phys_rows, scales, scale_block_size, indices, indices_stride, topk_lengths,
+             nullptr, T, H, softmax_scale, attn_sink, out, nsplit, nsplit > 1 ? part_o : nullptr, part_lse};
+  st = launch_attention(a, err, stream);
+  if (st != SMLA_OK || nsplit == 1) return st;
+  return launch_decode_combine(part_o, part_lse, attn_sink, T, H, nsplit, out, stream);
 }
 
 smla_status_t smla_check_device_errors(cudaStream_t stream) {

@@ -31,9 +31,11 @@
 //
 // Softmax: keys are TMEM lanes, so a head's maximum is a cross-lane
 // reduction (warp redux on order-preserving ints, then shared-memory atomic
-// max across the 4 lane quarters).  The reference maximum m is only raised
-// when a block exceeds it by more than 2^8 (lazy rescale), keeping P <= 256
-// inside the e4m3 range; raising it rescales O^T and the row sums.
+// max across the 4 lane quarters).  The reference m sits 2^4 below the
+// largest logit seen when it was set (so that the weights near the maximum
+// keep e4m3's precision) and is only raised when a block exceeds it by more
+// than 2^8 (lazy rescale), keeping P <= 256 inside the e4m3 range; raising
+// it rescales O^T and the row sums.
 //
 // Pipeline: NST gather slots (2 when they fit in shared memory).  The
 // producers fetch the next block's row indices and scales while the current
@@ -95,10 +97,25 @@ static_assert(kSoftWarps % 4 == 0 && kMmaWarp % 4 == 0, "roles must split on war
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 256;  // S^T accumulators from 256; O^T tiles at [0, 256)
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kTau = 8.0f;      // lazy-rescale threshold (log2 units)
+constexpr float kTau = 8.0f;      // lazy-rescale threshold (log2 units): P stays <= 2^8
+// The reference a head's weights are taken against sits this far (log2
+// units) below the largest logit seen when it was set, so that the block
+// maximum's weight is 2^4 rather than 1.  The two-term (hi + lo) e4m3 P then
+// keeps about 2^-8 relative precision for weights down to 2^-6 of the
+// maximum (with the maximum at 1, lo fell below e4m3's normal range, 2^-6,
+// for weights under 2^-2 of it, and those weights carried an absolute error
+// of about 2^-10).  A later block rescales once it exceeds the reference by
+// 2^8, i.e. the previous maximum by 2^4.
+constexpr float kPOffset = 4.0f;
 constexpr int kOrdMin = static_cast<int>(0x80000000u);
 
 enum Scale { kUnit = 0, kRow = 1, kBlock = 2 };
+
+// Where a token's keys come from.
+enum Keys {
+  kIndexed = 0,  // sparse: indices[t, 0 .. topk_lengths[t]) (physical rows)
+  kCausal = 1,   // dense: every logical key 0..pos(t) of t's sequence, through the page table
+};
 
 struct Params {
   const void* q;
@@ -114,6 +131,23 @@ struct Params {
   uint16_t* out;
   unsigned* err;
   int q_box3d;  // q tensor map is 3-D: one load brings all column boxes of an item
+  int keys;     // Keys
+  // kCausal: the ragged batch (smla_seqs_t)
+  const int32_t* cu_q;
+  const int32_t* kv_len;
+  const int32_t* page_table;
+  int B, max_pages, page_shift;
+  // attention sink: one logit per head (natural-log units, like the scaled
+  // logits) that joins every softmax denominator and carries no value; null
+  // for none
+  const float* sink;
+  // split-K: a token's key blocks are divided among nsplit work items, each
+  // writing its normalised partial output (f32) and log2-sum-exp per head
+  // to part_o [T, nsplit, H, 512] / part_lse [T, nsplit, H]; nsplit == 1
+  // writes the bf16 output directly
+  int nsplit;
+  float* part_o;
+  float* part_lse;
 };
 
 template <int QP, int KVP, int PP, int NST>
@@ -269,27 +303,72 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t a0, uint64_t 
       }
 }
 
-// One work item: a token and one group of 64 heads.
+// One work item: a token, one group of 64 heads and (split-K) one range of
+// the token's key blocks.
 struct Item {
-  int t, h0, hv, n, nblk;
+  int t, h0, hv;
+  int n;     // the token's keys (all splits)
+  int j0;    // first key block of this item
+  int nblk;  // key blocks of this item (0: nothing to attend to)
+  int s;     // split index
+  int b;     // sequence of the token (kCausal)
 };
-// item w from its token's selection length
-__device__ __forceinline__ Item item_make(const Params& p, int w, int groups, uint32_t len) {
-  Item it;
-  it.t = w / groups;
-  it.h0 = (w % groups) * kNH;
-  it.hv = min(kNH, p.H - it.h0);
-  int n = static_cast<int>(len);
+__device__ __forceinline__ int item_token(const Params& p, int w, int groups) { return w / (groups * p.nsplit); }
+
+// Sequence of token t (kCausal): the last b with cu_q[b] <= t.
+__device__ __forceinline__ int seq_of(const Params& p, int t) {
+  int lo = 0, hi = p.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.cu_q[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// The token's key count: its selection length (kIndexed) or pos + 1
+// (kCausal); `b` receives the sequence for kCausal.
+template <int KEYS>
+__device__ __forceinline__ int token_keys(const Params& p, int t, int& b) {
+  if (KEYS == kCausal) {
+    b = seq_of(p, t);
+    const int q_len = p.cu_q[b + 1] - p.cu_q[b];
+    const int n = p.kv_len[b] - q_len + (t - p.cu_q[b]) + 1;
+    if (n < 0 || n > (p.max_pages << p.page_shift)) {
+      if (threadIdx.x == 0) atomicOr(p.err, kErrShape);
+      return 0;
+    }
+    return n;
+  }
+  b = 0;
+  int n = static_cast<int>(p.lens[t]);
   if (n > p.indices_stride) {
     if (threadIdx.x == 0) atomicOr(p.err, kErrShape);
     n = p.indices_stride;
   }
+  return n;
+}
+
+// item w given its token's key count n (and sequence b)
+__device__ __forceinline__ Item item_make(const Params& p, int w, int groups, int n, int b) {
+  Item it;
+  const int tg = w / p.nsplit;
+  it.s = w - tg * p.nsplit;
+  it.t = tg / groups;
+  it.h0 = (tg % groups) * kNH;
+  it.hv = min(kNH, p.H - it.h0);
   it.n = n;
-  it.nblk = (n + kBK - 1) / kBK;
+  it.b = b;
+  const int nb = (n + kBK - 1) / kBK;
+  const int per = (nb + p.nsplit - 1) / p.nsplit;
+  it.j0 = min(nb, it.s * per);
+  it.nblk = min(nb, it.j0 + per) - it.j0;
   return it;
 }
+template <int KEYS>
 __device__ __forceinline__ Item item_at(const Params& p, int w, int groups) {
-  return item_make(p, w, groups, p.lens[w / groups]);
+  int b;
+  const int n = token_keys<KEYS>(p, item_token(p, w, groups), b);
+  return item_make(p, w, groups, n, b);
 }
 
 // Persistent CTAs: CTA c takes the work items c, c + gridDim.x, ... in turn,
@@ -297,7 +376,7 @@ __device__ __forceinline__ Item item_at(const Params& p, int w, int groups) {
 // phases come from its index g over all of this CTA's blocks), so the next
 // item's first rows are gathered, and its q split, while the current item's
 // last blocks and epilogue run.
-template <int QP, int KVP, int PP, int NST, int SC>
+template <int QP, int KVP, int PP, int NST, int SC, int KEYS>
 __global__ void __launch_bounds__(threads_for(KVP), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const Params p) {
   using S = Smem<QP, KVP, PP, NST>;
@@ -326,7 +405,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
   }
   S& s = *reinterpret_cast<S*>(smem_raw);
   const int groups = (p.H + kNH - 1) / kNH;
-  const int items = p.T * groups;
+  const int items = p.T * groups * p.nsplit;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&s.bar_qraw), 1);
@@ -449,21 +528,32 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     int gb = 0;  // index of the item's first block among this CTA's blocks
     bool ok = true;
     bool q_in = false;  // s.q holds the current item's converted q
-    Item I = item_at(p, blockIdx.x, groups);
+    Item I = item_at<KEYS>(p, blockIdx.x, groups);
     for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
       const int wn = w + static_cast<int>(gridDim.x);  // this CTA's next item
       const int n = I.n, nblk = I.nblk;
       uint16_t* out_t = p.out + (static_cast<int64_t>(I.t) * p.H + I.h0) * kDV;
-      if (n == 0) {  // empty selection: zeros (no softmax mass); the QK warp skips it
-        for (int i = threadIdx.x; i < I.hv * kDV / 8; i += kSoftThreads)
-          __stcs(reinterpret_cast<uint4*>(out_t) + i, make_uint4(0, 0, 0, 0));
-        if (wn < items) I = item_at(p, wn, groups);
+      // split-K partials of this item: rows (t * nsplit + s) * H + h of
+      // [T, nsplit, H, 512] and [T, nsplit, H]
+      auto part_row = [&]() { return (static_cast<int64_t>(I.t) * p.nsplit + I.s) * p.H + I.h0; };
+      if (nblk == 0) {
+        // nothing to attend to: zeros (no softmax mass), or for a split an
+        // empty partial (log-sum-exp -inf, which the combine skips); the QK
+        // warp skips the item
+        if (p.nsplit > 1) {
+          if (threadIdx.x < I.hv) p.part_lse[part_row() + threadIdx.x] = -INFINITY;
+        } else {
+          for (int i = threadIdx.x; i < I.hv * kDV / 8; i += kSoftThreads)
+            __stcs(reinterpret_cast<uint4*>(out_t) + i, make_uint4(0, 0, 0, 0));
+        }
+        if (wn < items) I = item_at<KEYS>(p, wn, groups);
         continue;
       }
       if (!q_in && !convert_q(I)) { ok = false; break; }  // first item, or after an empty one
       q_in = false;
-      // selection length of item wn: loaded now, used by the epilogue
-      const uint32_t len_next = wn < items ? p.lens[wn / groups] : 0u;
+      // key count of item wn's token: loaded now, used by the epilogue
+      int b_next = 0;
+      const int n_next = wn < items ? token_keys<KEYS>(p, item_token(p, wn, groups), b_next) : 0;
       if (threadIdx.x < kNH) s.negm[threadIdx.x] = 0.f;  // block 0 sets the reference
       named_bar_sync(1, kSoftThreads);
       // lv[h]: this key lane's share of head hb+h's softmax denominator,
@@ -536,7 +626,8 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
             }
           }
         }
-        if ((j + 1) * kBK > n && j * kBK + r >= n) {  // lanes past the selection (last block only)
+        const int jg = I.j0 + j;  // block index among the token's blocks
+        if ((jg + 1) * kBK > n && jg * kBK + r >= n) {  // lanes past the token's keys (its last block only)
 #pragma unroll
           for (int h = 0; h < 32; ++h) y[h] = -INFINITY;
           ymax = -INFINITY;
@@ -544,9 +635,10 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         // Fast path: no element exceeds its head's reference by more than tau.
         if (named_bar_or(1, kSoftThreads, j == 0 || ymax + lg > kTau)) {
           // Slow path (always taken by block 0): t_h = block maximum of y + lg
-          // per head across the 128 key lanes.  Block 0 sets m_h = t_h; a
-          // later block raises m_h by t_h where t_h > tau and scales O^T and
-          // the row sums of that head by exp2(-t_h).
+          // per head across the 128 key lanes.  Block 0 sets m_h = t_h -
+          // kPOffset; a later block raises m_h by d_h = t_h - kPOffset where
+          // t_h > tau and scales O^T and the row sums of that head by
+          // exp2(-d_h).
           int mine = kOrdMin;
 #pragma unroll
           for (int h = 0; h < 32; ++h) {
@@ -561,9 +653,9 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
             s.mx[hh] = kOrdMin;
             float d = 0.f, f = 1.f;
             if (j == 0 || t > kTau) {
-              d = t;
-              if (j > 0) f = exp2f(-t);
-              s.negm[hh] -= t;
+              d = t - kPOffset;
+              if (j > 0) f = exp2f(-d);
+              s.negm[hh] -= d;
             }
             s.delta[hh] = d;
             s.fac[hh] = f;
@@ -659,8 +751,8 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
       // overlaps this epilogue
       Item In{};
       if (wn < items) {
-        In = item_make(p, wn, groups, len_next);
-        if (In.n > 0) {
+        In = item_make(p, wn, groups, n_next, b_next);
+        if (In.nblk > 0) {
           if (!convert_q(In)) { ok = false; break; }
           q_in = true;
         }
@@ -668,11 +760,32 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
       // ---- O^T / l -> bf16 once the last PV has completed
       const bool done = named_bar_and(1, kSoftThreads, mbar_wait(smem_u32(&s.bar_pv_done), (gb - 1) & 1, p.err));
       if (threadIdx.x < kNH) {
-        const float l = linv[threadIdx.x];
+        // l = sum_j exp2(z_j - m); the reference m is -negm (log2 units)
+        float l = linv[threadIdx.x];
+        if (p.nsplit > 1) {
+          // split partial: log2-sum-exp m + log2 l (the combine adds the sink)
+          if (threadIdx.x < I.hv) p.part_lse[part_row() + threadIdx.x] = l > 0.f ? log2f(l) - s.negm[threadIdx.x] : -INFINITY;
+        } else if (p.sink != nullptr && threadIdx.x < I.hv) {
+          l += ex2_approx(fmaf(p.sink[I.h0 + threadIdx.x], kLog2e, s.negm[threadIdx.x]));
+        }
         linv[threadIdx.x] = l > 0.f ? 1.f / l : 0.f;
       }
       named_bar_sync(1, kSoftThreads);
-      if (done) {
+      if (done && p.nsplit > 1) {
+        tc_fence_after();
+        // normalised partial O, f32: thread = one value column, a warp store
+        // covers 32 consecutive columns of one head
+        float* po = p.part_o + part_row() * kDV + r;
+#pragma unroll 1
+        for (int tile = 0; tile < 4; ++tile) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + tile * kNH + hb, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 32; ++h)
+            if (hb + h < I.hv) __stcs(po + static_cast<int64_t>(hb + h) * kDV + tile * 128, __uint_as_float(v[h]) * linv[hb + h]);
+        }
+      } else if (done) {
         tc_fence_after();
         // thread = one value column.  Lane pairs swap one value per two heads,
         // so the even lane holds columns (c, c+1) of head h and the odd lane
@@ -721,7 +834,8 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     auto issue_q = [&](int w) {
       ++q_issued;
       if (leader) {
-        const int row = w / groups * p.H + (w % groups) * kNH;
+        const int tg = w / p.nsplit;  // (token, head group) of item w
+        const int row = tg / groups * p.H + (tg % groups) * kNH;
         mbar_arrive_expect_tx(smem_u32(&s.bar_qraw), kQBoxes * kNH * 64);
         if (p.q_box3d) {
           tma_load_3d_hint(smem_u32(s.q), &tq, 0, row, 0, smem_u32(&s.bar_qraw), q_policy);
@@ -735,18 +849,18 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     };
     auto next_nonempty = [&](int w) {
       for (w += gridDim.x; w < items; w += gridDim.x)
-        if (item_at(p, w, groups).n > 0) return w;
+        if (item_at<KEYS>(p, w, groups).nblk > 0) return w;
       return items;
     };
     int qn = 0, gb = 0;
     bool ok = true;
     {
-      const int w0 = item_at(p, blockIdx.x, groups).n > 0 ? static_cast<int>(blockIdx.x) : next_nonempty(blockIdx.x);
+      const int w0 = item_at<KEYS>(p, blockIdx.x, groups).nblk > 0 ? static_cast<int>(blockIdx.x) : next_nonempty(blockIdx.x);
       if (w0 < items) issue_q(w0);
     }
     for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
-      const Item I = item_at(p, w, groups);
-      if (I.n == 0) continue;
+      const Item I = item_at<KEYS>(p, w, groups);
+      if (I.nblk == 0) continue;
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_q), qn & 1, p.err));
       ++qn;
       for (int j = 0; ok && j < I.nblk; ++j) {
@@ -789,7 +903,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     int gb = 0;
     bool ok = true;
     for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
-      const Item I = item_at(p, w, groups);
+      const Item I = item_at<KEYS>(p, w, groups);
       for (int j = 0; j < I.nblk; ++j) {
         const int g = gb + j;
         // O^T[512 vcols x 64 heads] += V^T P^T over the block's 128 keys, one
@@ -838,23 +952,42 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     bool ok = true;
     int gb = 0;
     for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
-      const Item I = item_at(p, w, groups);
+      const Item I = item_at<KEYS>(p, w, groups);
       const int n = I.n;
-      if (n == 0) continue;
+      if (I.nblk == 0) continue;
       const uint32_t* tok_idx = p.indices + static_cast<int64_t>(I.t) * p.indices_stride;
-      const uint32_t first = tok_idx[0];
+      const int32_t* pages = p.page_table + static_cast<int64_t>(I.b) * p.max_pages;
+      // physical row of the token's key i: its index (kIndexed) or its
+      // logical key through the page table (kCausal); out-of-range rows are
+      // reported and replaced by row 0
+      auto key_row = [&](int i) -> uint32_t {
+        int64_t row;
+        if (KEYS == kCausal) {
+          const int pid = pages[i >> p.page_shift];
+          row = (static_cast<int64_t>(pid) << p.page_shift) | (i & ((1 << p.page_shift) - 1));
+          if (pid < 0 || row >= p.phys_rows) {
+            atomicOr(p.err, kErrPage);
+            row = 0;
+          }
+        } else {
+          row = tok_idx[i];
+          if (row >= p.phys_rows) {
+            atomicOr(p.err, kErrIndex);
+            row = 0;
+          }
+        }
+        return static_cast<uint32_t>(row);
+      };
+      // lanes past the token's keys gather its key 0 again (finite values
+      // that the softmax weights by zero)
+      const uint32_t first = pt < kBK ? key_row(0) : 0u;
       // Thread pt < 128 owns row pt of every block: its physical row (and
       // tensorwise scale) are loaded one block ahead.
       uint32_t nxt_row = 0;
       float nxt_sr = 1.f;
       auto load_row = [&](int jb) {
-        const int key = jb * kBK + pt;
-        uint32_t row = key < n ? tok_idx[key] : first;
-        if (row >= static_cast<uint64_t>(p.phys_rows)) {
-          atomicOr(p.err, kErrIndex);
-          row = 0;
-        }
-        nxt_row = row;
+        const int key = (I.j0 + jb) * kBK + pt;
+        nxt_row = key < n ? key_row(key) : first;
       };
       auto load_scale = [&]() {  // block scales are gathered with the rows
         if (SC == kRow) nxt_sr = p.scales[static_cast<int64_t>(nxt_row) * p.nscale];
@@ -943,54 +1076,87 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int QP, int KVP, int PP, int NST, int SC>
-static smla_status_t launch_t(const CUtensorMap& tq, const Params& p, cudaStream_t stream) {
+template <int QP, int KVP, int PP, int NST, int SC, int KEYS>
+static smla_status_t launch_k(const CUtensorMap& tq, const Params& p, cudaStream_t stream) {
   const size_t smem = sizeof(Smem<QP, KVP, PP, NST>);
   static_assert(sizeof(Smem<QP, KVP, PP, NST>) <= 232448, "the variant's shared memory exceeds a CTA's 227 KB");
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<QP, KVP, PP, NST, SC>,
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<QP, KVP, PP, NST, SC, KEYS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return fail_cuda(e, "prefill smem attribute");
   // The register split (setmaxnreg) draws on the launch allocation: refuse a
   // build whose register count would leave the softmax's increase waiting.
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, prefill_kernel<QP, KVP, PP, NST, SC>);
+  e = cudaFuncGetAttributes(&fa, prefill_kernel<QP, KVP, PP, NST, SC, KEYS>);
   if (e != cudaSuccess) return fail_cuda(e, "prefill attributes");
   if (fa.numRegs != kLaunchRegs)
     return fail(SMLA_ERR_UNSUPPORTED, "prefill kernel built with %d registers a thread, the register split needs %d",
                 fa.numRegs, kLaunchRegs);
   // persistent: one CTA per SM (shared memory allows no more), at most one per item
-  const int64_t items = static_cast<int64_t>(p.T) * ((p.H + kNH - 1) / kNH);
+  const int64_t items = static_cast<int64_t>(p.T) * ((p.H + kNH - 1) / kNH) * p.nsplit;
   const dim3 grid(static_cast<unsigned>(std::min<int64_t>(items, device_sm_count())));
-  prefill_kernel<QP, KVP, PP, NST, SC><<<grid, threads_for(KVP), smem, stream>>>(tq, p);
+  prefill_kernel<QP, KVP, PP, NST, SC, KEYS><<<grid, threads_for(KVP), smem, stream>>>(tq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, "prefill launch");
   return SMLA_OK;
 }
 
+template <int QP, int KVP, int PP, int NST, int SC>
+static smla_status_t launch_t(const CUtensorMap& tq, const Params& p, cudaStream_t stream) {
+  return p.keys == kCausal ? launch_k<QP, KVP, PP, NST, SC, kCausal>(tq, p, stream)
+                           : launch_k<QP, KVP, PP, NST, SC, kIndexed>(tq, p, stream);
+}
+
 }  // namespace pf
 
-smla_status_t launch_sparse_prefill(const void* q, int q_dtype, const uint8_t* latent, int64_t phys_rows,
-                                    const float* scales, int sbs, const uint32_t* indices, int indices_stride,
-                                    const uint32_t* topk_lengths, int T, int H, float softmax_scale, uint16_t* out,
-                                    unsigned* err, cudaStream_t stream) {
+smla_status_t launch_attention(const AttnArgs& a, unsigned* err, cudaStream_t stream) {
   using namespace pf;
+  const int sbs = a.sbs;
   const int nscale = sbs == 0 ? 0 : (kD + sbs - 1) / sbs;
-  Params p{q, latent, phys_rows, scales, nscale, indices, indices_stride, topk_lengths, T, H, softmax_scale, out, err, 0};
-  const bool bf16 = q_dtype == SMLA_BF16;
+  Params p{};
+  p.q = a.q;
+  p.latent = a.latent;
+  p.phys_rows = a.phys_rows;
+  p.scales = a.scales;
+  p.nscale = nscale;
+  p.indices = a.indices;
+  p.indices_stride = a.indices_stride;
+  p.lens = a.topk_lengths;
+  p.T = a.T;
+  p.H = a.H;
+  p.softmax_scale = a.softmax_scale;
+  p.out = a.out;
+  p.err = err;
+  p.sink = a.sink;
+  p.nsplit = a.nsplit < 1 ? 1 : a.nsplit;
+  p.part_o = a.part_o;
+  p.part_lse = a.part_lse;
+  if (a.seqs) {
+    p.keys = kCausal;
+    p.cu_q = a.seqs->cu_q;
+    p.kv_len = a.seqs->kv_len;
+    p.page_table = a.seqs->page_table;
+    p.B = a.seqs->B;
+    p.max_pages = a.seqs->max_pages;
+    p.page_shift = __builtin_ctz(static_cast<unsigned>(a.seqs->page_size));
+  } else {
+    p.keys = kIndexed;
+  }
+  const bool bf16 = a.q_dtype == SMLA_BF16;
   if (bf16 && sbs != 0 && sbs < kD) return fail(SMLA_ERR_UNSUPPORTED, "bf16 q with block scales is not built (shared memory)");
   // q rows [T * H] x (576 elements) as bytes, loaded as 64-byte column boxes
   // of 64 rows: preferably one 3-D box (x = byte in the box, y = row, z =
   // box index with a 64-byte stride), else a 2-D map with one load per box.
   CUtensorMap tq;
+  const int T = a.T, H = a.H;
   const uint64_t pitch = static_cast<uint64_t>(kD) * (bf16 ? 2 : 1);
   const uint32_t nbox = static_cast<uint32_t>(pitch / 64);
   {
     const uint64_t dims[3] = {64, static_cast<uint64_t>(T) * H, nbox};
     const uint64_t strides[2] = {pitch, 64};
     const uint32_t box[3] = {64, static_cast<uint32_t>(kNH), nbox};
-    p.q_box3d = encode_tma_u8(&tq, q, 3, dims, strides, box, 64) ? 1 : 0;
+    p.q_box3d = encode_tma_u8(&tq, a.q, 3, dims, strides, box, 64) ? 1 : 0;
   }
-  if (!p.q_box3d && !encode_tma_2d_u8(&tq, q, pitch, static_cast<uint64_t>(T) * H, 64, kNH, 64))
+  if (!p.q_box3d && !encode_tma_2d_u8(&tq, a.q, pitch, static_cast<uint64_t>(T) * H, 64, kNH, 64))
     return fail(SMLA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the prefill q tensor map");
   if (sbs == 0) return bf16 ? launch_t<2, 1, 2, 2, kUnit>(tq, p, stream) : launch_t<1, 1, 1, 2, kUnit>(tq, p, stream);
   if (sbs >= kD) return bf16 ? launch_t<2, 1, 2, 2, kRow>(tq, p, stream) : launch_t<1, 1, 1, 2, kRow>(tq, p, stream);

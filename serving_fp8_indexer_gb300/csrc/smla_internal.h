@@ -34,9 +34,36 @@ smla_status_t launch_indexer(const uint8_t* q, const float* q_scale, const uint8
 smla_status_t launch_topk(const float* scores, int64_t score_stride, const smla_seqs_t& seqs, int k,
                           uint32_t* indices, uint32_t* topk_lengths, unsigned* err, cudaStream_t stream);
 
-smla_status_t launch_sparse_prefill(const void* q, int q_dtype, const uint8_t* latent, int64_t phys_rows,
-                                    const float* scales, int sbs, const uint32_t* indices, int indices_stride,
-                                    const uint32_t* topk_lengths, int T, int H, float softmax_scale,
-                                    uint16_t* out, unsigned* err, cudaStream_t stream);
+// One launch of the attention kernel: sparse (indices + lengths) or dense
+// causal (seqs non-null: every key 0..pos through the page table), with an
+// optional per-head sink and, for nsplit > 1, split-K partials instead of
+// the bf16 output.
+struct AttnArgs {
+  const void* q;
+  int q_dtype;
+  const uint8_t* latent;
+  int64_t phys_rows;
+  const float* scales;
+  int sbs;
+  const uint32_t* indices;
+  int indices_stride;
+  const uint32_t* topk_lengths;
+  const smla_seqs_t* seqs;
+  int T, H;
+  float softmax_scale;
+  const float* sink;
+  uint16_t* out;
+  int nsplit;
+  float* part_o;    // [T, nsplit, H, 512]
+  float* part_lse;  // [T, nsplit, H]
+};
+smla_status_t launch_attention(const AttnArgs& a, unsigned* err, cudaStream_t stream);
+
+// Split-K decode: the split count for these sizes, the workspace it needs,
+// and the kernel that combines the partials into the bf16 output.
+int decode_splits(int T, int H, int indices_stride);
+size_t decode_workspace_bytes(int T, int H, int nsplit);
+smla_status_t launch_decode_combine(const float* part_o, const float* part_lse, const float* sink, int T, int H,
+                                    int nsplit, uint16_t* out, cudaStream_t stream);
 
 }  // namespace smla

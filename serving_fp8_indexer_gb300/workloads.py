@@ -254,3 +254,18 @@ def e2e_chunk(seed=4, B=8, L=8192, q_len=2048, k=2048, H=128, h_idx=64) -> Workl
     bf16 Q, tensorwise-scaled e4m3 latent (one scale per row)."""
     return build(f"e2e_chunk_B{B}_L{L}_q{q_len}_H{H}_k{k}", seed, [q_len] * B, [L] * B, 64,
                  h_idx=h_idx, topk=k, H=H, q_dtype=Q_BF16, sbs=QK_DEPTH)
+
+
+def sparse_decode(seed=5, B=8, q_per_seq=2, L=8192, k=2048, H=128, q_dtype=Q_BF16, sbs=0) -> Workload:
+    """Sparse MLA decode: B sequences of L cached tokens with q_per_seq new
+    tokens each (the last positions, as in MTP decode), top-k causally
+    sampled indices, H heads."""
+    return build(f"sparse_decode_B{B}x{q_per_seq}_L{L}_H{H}_k{k}_{'bf16' if q_dtype == Q_BF16 else 'fp8'}_sbs{sbs}",
+                 seed, [q_per_seq] * B, [L] * B, 64, topk=k, H=H, q_dtype=q_dtype, sbs=sbs, sample_indices=True)
+
+
+def dense_prefill(seed=6, lens=(512, 1024, 2048, 1537), H=128, q_dtype=Q_BF16, sbs=0) -> Workload:
+    """Dense causal prefill of short prompts: every token attends to all of
+    its sequence's keys 0..pos (no indices), H heads."""
+    return build(f"dense_prefill_{'-'.join(map(str, lens))}_H{H}_{'bf16' if q_dtype == Q_BF16 else 'fp8'}_sbs{sbs}",
+                 seed, list(lens), list(lens), 64, H=H, q_dtype=q_dtype, sbs=sbs)

@@ -95,7 +95,7 @@ def test_prefill_validation(lib):
     assert call(sbs=64) == UNSUPPORTED and "scale_block_size" in _msg(lib)
     assert call(sbs=32, qd=1) == INVALID and "scales" in _msg(lib)
     assert call(sbs=32, sc=P) == UNSUPPORTED and "e4m3 q" in _msg(lib)   # block scales need e4m3 q
-    assert call(sink=P) == UNSUPPORTED and "attn_sink" in _msg(lib)
+    assert call(sink=P + 2) == INVALID and "attn_sink" in _msg(lib)   # the sink is f32 [H], 4-byte aligned
     assert call(ss=float("nan")) == INVALID
     assert call(st=0) == INVALID
     assert call(out=None) == INVALID

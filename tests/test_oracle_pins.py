@@ -372,3 +372,61 @@ def test_attention_e4m3_q_branch():
         Q[None], K[None, None].expand(1, H, L, 576), K[None, None, :, :512].expand(1, H, L, 512),
         is_causal=True, scale=sc)[0].permute(1, 0, 2).numpy()
     assert np.allclose(out, ref, rtol=1e-11, atol=1e-13)
+
+
+def test_attention_sink_closed_forms():
+    """The sink reading pinned by closed forms: one key of logit s and sink
+    logit z give out = V * e^s / (e^s + e^z) = V * sigmoid(s - z); a sink of
+    -inf is no sink; two keys and a sink at the same logit give each key 1/3;
+    a very large sink drives the output to 0."""
+    rng = np.random.default_rng(31)
+    latent, q, idx = _attn_inputs(rng, 2, 3, 40, 6)
+    sc = 0.05
+    one = np.ones(2, np.uint32)
+    z = np.array([0.3, -1.2, 2.5])
+    out = oracle.sparse_prefill(q, 0, latent, None, 0, idx, one, sc, attn_sink=z)
+    for t in range(2):
+        K = oracle.decode_e4m3(latent[idx[t, 0]])
+        qf = oracle.decode_bf16(q[t])
+        for h in range(3):
+            s = sc * math.fsum(qf[h] * K)
+            w = 1.0 / (1.0 + math.exp(z[h] - s))
+            assert np.allclose(out[t, h], w * K[:512], rtol=1e-13, atol=1e-15)
+    lens = np.array([6, 4], np.uint32)
+    a = oracle.sparse_prefill(q, 0, latent, None, 0, idx, lens, sc)
+    b = oracle.sparse_prefill(q, 0, latent, None, 0, idx, lens, sc, attn_sink=np.full(3, -np.inf))
+    assert np.array_equal(a, b)
+    big = oracle.sparse_prefill(q, 0, latent, None, 0, idx, lens, sc, attn_sink=np.full(3, 1e4))
+    assert np.abs(big).max() == 0.0
+    # two identical rows (equal logits) and a sink at that logit: weights 1/3 each
+    lat2 = np.zeros((2, 576), np.uint8)
+    lat2[0] = lat2[1] = latent[0]
+    qz = np.zeros((1, 1, 576), np.uint16)   # q = 0: every logit 0
+    o3 = oracle.sparse_prefill(qz, 0, lat2, None, 0, np.array([[0, 1]], np.uint32), np.array([2], np.uint32), sc,
+                               attn_sink=np.zeros(1))
+    assert np.allclose(o3[0, 0], (2.0 / 3.0) * oracle.decode_e4m3(latent[0])[:512], rtol=1e-14, atol=0)
+
+
+def test_dense_prefill_equals_causal_sdpa_over_pages():
+    """The dense causal oracle on two paged sequences (new tokens at the end
+    of each) against float64 scaled_dot_product_attention with the causal
+    mask offset by the cached prefix, per sequence."""
+    rng = np.random.default_rng(33)
+    q_lens, kv_lens, ps, H = [5, 9], [12, 9], 4, 3
+    seqs = wl.make_seqs(rng, q_lens, kv_lens, ps)
+    lat = wl.to_e4m3_bytes(rng.standard_normal((seqs.phys_rows, 576)).astype(np.float32))
+    q = wl.to_bf16_bits(rng.standard_normal((seqs.T, H, 576)).astype(np.float32))
+    sc = 1 / math.sqrt(576)
+    out = oracle.dense_prefill(q, 0, lat, None, 0, seqs.cu_q, seqs.kv_len, seqs.page_table, ps, sc)
+    for b in range(2):
+        a, e = int(seqs.cu_q[b]), int(seqs.cu_q[b + 1])
+        L = int(seqs.kv_len[b])
+        rows = wl.logical_to_phys(seqs, b, np.arange(L))
+        K = torch.from_numpy(lat[rows]).view(torch.float8_e4m3fn).double()
+        Q = torch.from_numpy(q[a:e].view(np.int16)).view(torch.bfloat16).double().permute(1, 0, 2)
+        pos = L - (e - a) + np.arange(e - a)
+        mask = torch.from_numpy(np.arange(L)[None, :] <= pos[:, None])
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            Q[None], K[None, None].expand(1, H, L, 576), K[None, None, :, :512].expand(1, H, L, 512),
+            attn_mask=mask, scale=sc)[0].permute(1, 0, 2).numpy()
+        assert np.allclose(out[a:e], ref, rtol=1e-11, atol=1e-13)
