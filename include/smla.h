@@ -182,6 +182,35 @@ smla_status_t smla_sparse_decode(const void* q, int32_t q_dtype, const uint8_t* 
                                  uint16_t* out, void* workspace, size_t workspace_bytes,
                                  cudaStream_t stream);
 
+/* smla_sparse_decode without a workspace, for callers that cannot allocate
+ * device memory at the point where they decode: code running inside another
+ * runtime's enqueue step that forbids allocation (an inference-engine
+ * plugin, say), or a serving loop whose device memory is all reserved by a
+ * pool it may not go around, or where a cudaMalloc would stall the loop.
+ * The papers have no counterpart of this call; it is an integration
+ * convenience.
+ * Same arguments, result and rules as smla_sparse_decode, minus workspace
+ * and workspace_bytes: the split partials live in a fixed 32 MiB scratch
+ * array that the library declares in device memory.  Every GPU that loads
+ * the library holds those 32 MiB until the process exits.  The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * The first call on a device looks the array's device address up (once,
+ * with that device current) and should come before any stream capture.
+ * The split count is the one smla_sparse_decode uses; on a 152-SM GB300 it
+ * never needs more than about 20 MB.  Sizes that would need more than 32 MiB
+ * return SMLA_ERR_UNSUPPORTED with a message naming the need, and nothing
+ * is launched.  All calls share the one array, which keeps the last call's
+ * contents; every entry a call reads back is written first by that call, so
+ * nothing has to start at zero.  Calls whose kernels overlap on the GPU
+ * (different streams, or other host threads) race on the array: order them
+ * on one stream. */
+smla_status_t smla_sparse_decode_noalloc(const void* q, int32_t q_dtype, const uint8_t* latent_pool,
+                                         int64_t phys_rows, const float* scales, int32_t scale_block_size,
+                                         const uint32_t* indices, int32_t indices_stride,
+                                         const uint32_t* topk_lengths, int32_t T, int32_t H,
+                                         int32_t v_depth, float softmax_scale, const float* attn_sink,
+                                         uint16_t* out, cudaStream_t stream);
+
 /* Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns SMLA_OK, SMLA_ERR_DEVICE_CHECK (out-of-range index or page
  * id), SMLA_ERR_TIMEOUT (a pipeline wait gave up) or SMLA_ERR_CUDA. */

@@ -16,6 +16,7 @@ from ._lib import (  # noqa: F401
     dense_prefill,
     sparse_decode_workspace_size,
     sparse_decode,
+    sparse_decode_noalloc,
     check_device_errors,
     selftest_wait_timeout,
     version,

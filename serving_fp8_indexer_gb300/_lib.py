@@ -26,6 +26,7 @@ SMLA_E4M3 = 1
 
 EXPORTED = ("smla_indexer_scores", "smla_topk_workspace_size", "smla_topk", "smla_sparse_prefill",
             "smla_dense_prefill", "smla_sparse_decode_workspace_size", "smla_sparse_decode",
+            "smla_sparse_decode_noalloc",
             "smla_check_device_errors", "smla_selftest_wait_timeout", "smla_last_error", "smla_version")
 
 
@@ -68,13 +69,16 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.smla_sparse_decode_workspace_size.restype = sz
         lib.smla_sparse_decode.argtypes = [vp, i32, vp, i64, vp, i32, vp, i32, vp, i32, i32, i32, f32, vp, vp, vp,
                                            sz, vp]
+        lib.smla_sparse_decode_noalloc.argtypes = [vp, i32, vp, i64, vp, i32, vp, i32, vp, i32, i32, i32, f32, vp,
+                                                   vp, vp]
         lib.smla_sparse_prefill.argtypes = [vp, i32, vp, i64, vp, i32, vp, i32, vp, i32, i32, i32, f32, vp, vp, vp]
         lib.smla_check_device_errors.argtypes = [vp]
         lib.smla_last_error.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
         lib.smla_last_error.restype = ctypes.c_size_t
         lib.smla_version.restype = ctypes.c_char_p
         for name in ("smla_indexer_scores", "smla_topk", "smla_sparse_prefill", "smla_dense_prefill",
-                     "smla_sparse_decode", "smla_check_device_errors", "smla_selftest_wait_timeout"):
+                     "smla_sparse_decode", "smla_sparse_decode_noalloc", "smla_check_device_errors",
+                     "smla_selftest_wait_timeout"):
             getattr(lib, name).restype = ctypes.c_int
         if path is None:
             _lib = lib
@@ -240,6 +244,27 @@ def sparse_decode(q: torch.Tensor, latent: torch.Tensor, scales: Optional[torch.
                                 _ptr(topk_lengths, torch.uint32, "topk_lengths", 1), T, H, int(out.shape[2]),
                                 float(softmax_scale), _ptr(attn_sink, torch.float32, "attn_sink", 1),
                                 _ptr(out, torch.bfloat16, "out", 3), ws, wsb, _stream(stream))
+    _check(lib, st)
+    return out
+
+
+def sparse_decode_noalloc(q: torch.Tensor, latent: torch.Tensor, scales: Optional[torch.Tensor],
+                          scale_block_size: int, indices: torch.Tensor, topk_lengths: torch.Tensor,
+                          softmax_scale: float, out: torch.Tensor, attn_sink: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """sparse_decode for callers that cannot allocate device memory: no
+    workspace argument; the split partials use the library's fixed device
+    scratch (see smla_sparse_decode_noalloc in include/smla.h)."""
+    lib = load()
+    qd, qp = _q_arg(q)
+    T, H = int(q.shape[0]), int(q.shape[1])
+    st = lib.smla_sparse_decode_noalloc(qp, qd, _ptr(latent, torch.uint8, "latent", 2), int(latent.shape[0]),
+                                        _ptr(scales, torch.float32, "scales", 2), int(scale_block_size),
+                                        _ptr(indices, torch.uint32, "indices", 2), int(indices.shape[1]),
+                                        _ptr(topk_lengths, torch.uint32, "topk_lengths", 1), T, H,
+                                        int(out.shape[2]), float(softmax_scale),
+                                        _ptr(attn_sink, torch.float32, "attn_sink", 1),
+                                        _ptr(out, torch.bfloat16, "out", 3), _stream(stream))
     _check(lib, st)
     return out
 

@@ -291,17 +291,29 @@ size_t smla_sparse_decode_workspace_size(int32_t T, int32_t H, int32_t indices_s
   return decode_workspace_bytes(T, H, decode_splits(T, H, indices_stride));
 }
 
-smla_status_t smla_sparse_decode(const void* q, int32_t q_dtype, const uint8_t* latent_pool, int64_t phys_rows,
-                                 const float* scales, int32_t scale_block_size, const uint32_t* indices,
-                                 int32_t indices_stride, const uint32_t* topk_lengths, int32_t T, int32_t H,
-                                 int32_t v_depth, float softmax_scale, const float* attn_sink, uint16_t* out,
-                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace smla {
+// smla_sparse_decode, and with use_static the allocation-free variant whose
+// split partials go to the library's fixed device scratch instead of a
+// caller workspace.
+static smla_status_t sparse_decode_impl(const void* q, int32_t q_dtype, const uint8_t* latent_pool,
+                                        int64_t phys_rows, const float* scales, int32_t scale_block_size,
+                                        const uint32_t* indices, int32_t indices_stride,
+                                        const uint32_t* topk_lengths, int32_t T, int32_t H, int32_t v_depth,
+                                        float softmax_scale, const float* attn_sink, uint16_t* out, void* workspace,
+                                        size_t workspace_bytes, bool use_static, cudaStream_t stream) {
   g_last_error.clear();
   smla_status_t st = check_attn(q, q_dtype, latent_pool, phys_rows, scales, scale_block_size, true, indices,
                                 indices_stride, topk_lengths, T, H, v_depth, softmax_scale, attn_sink, out);
   if (st != SMLA_OK) return st;
   const int nsplit = T > 0 ? decode_splits(T, H, indices_stride) : 1;
   const size_t need = decode_workspace_bytes(T, H, nsplit);
+  if (use_static && T > 0) {
+    st = noalloc_scratch_for(need, &workspace);
+    if (st != SMLA_OK) return st;
+    workspace_bytes = need;
+  }
   if (workspace_bytes < need || (need && !workspace))
     return fail(SMLA_ERR_INVALID_ARG, "workspace: %zu bytes given, %zu needed", workspace_bytes, need);
   if (workspace && !aligned16(workspace)) return fail(SMLA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
@@ -319,6 +331,30 @@ smla_status_t smla_sparse_decode(const void* q, int32_t q_dtype, const uint8_t* 
   st = launch_attention(a, err, stream);
   if (st != SMLA_OK || nsplit == 1) return st;
   return launch_decode_combine(part_o, part_lse, attn_sink, T, H, nsplit, out, stream);
+}
+
+}  // namespace smla
+
+extern "C" {
+
+smla_status_t smla_sparse_decode(const void* q, int32_t q_dtype, const uint8_t* latent_pool, int64_t phys_rows,
+                                 const float* scales, int32_t scale_block_size, const uint32_t* indices,
+                                 int32_t indices_stride, const uint32_t* topk_lengths, int32_t T, int32_t H,
+                                 int32_t v_depth, float softmax_scale, const float* attn_sink, uint16_t* out,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return sparse_decode_impl(q, q_dtype, latent_pool, phys_rows, scales, scale_block_size, indices, indices_stride,
+                            topk_lengths, T, H, v_depth, softmax_scale, attn_sink, out, workspace, workspace_bytes,
+                            false, stream);
+}
+
+smla_status_t smla_sparse_decode_noalloc(const void* q, int32_t q_dtype, const uint8_t* latent_pool,
+                                         int64_t phys_rows, const float* scales, int32_t scale_block_size,
+                                         const uint32_t* indices, int32_t indices_stride,
+                                         const uint32_t* topk_lengths, int32_t T, int32_t H, int32_t v_depth,
+                                         float softmax_scale, const float* attn_sink, uint16_t* out,
+                                         cudaStream_t stream) {
+  return sparse_decode_impl(q, q_dtype, latent_pool, phys_rows, scales, scale_block_size, indices, indices_stride,
+                            topk_lengths, T, H, v_depth, softmax_scale, attn_sink, out, nullptr, 0, true, stream);
 }
 
 smla_status_t smla_check_device_errors(cudaStream_t stream) {

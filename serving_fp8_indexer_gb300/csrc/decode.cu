@@ -11,6 +11,7 @@
 // M the largest of the L_s (and of the sink term), which equals the softmax
 // over all of the token's keys (and the sink) in one pass.
 #include <algorithm>
+#include <mutex>
 
 #include "ptx.cuh"
 #include "smla_internal.h"
@@ -58,6 +59,14 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const float* __restri
   reinterpret_cast<uint2*>(out + static_cast<int64_t>(row) * kDV)[threadIdx.x] = v;
 }
 
+// Scratch for smla_sparse_decode_noalloc: the split partials of one call
+// live here instead of in a caller-provided workspace.  Every GPU that loads
+// the library holds these bytes until the process exits.  Host code must not
+// use the array's name as a device address: it is a host-side stand-in; the
+// device address comes from cudaGetSymbolAddress (noalloc_scratch below).
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
 }  // namespace dec
 
 int decode_splits(int T, int H, int indices_stride) {
@@ -90,6 +99,40 @@ smla_status_t launch_decode_combine(const float* part_o, const float* part_lse, 
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, "decode combine launch");
   return SMLA_OK;
+}
+
+// Device address of the static scratch on the current device, looked up
+// once per device (with that device current) and cached.
+static smla_status_t noalloc_scratch(void** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(SMLA_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, dec::g_noalloc_scratch);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(decode scratch)");
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return SMLA_OK;
+}
+
+size_t noalloc_scratch_bytes() { return dec::kNoAllocScratchBytes; }
+
+smla_status_t noalloc_scratch_for(size_t need, void** out) {
+  if (need > dec::kNoAllocScratchBytes)
+    return fail(SMLA_ERR_UNSUPPORTED,
+                "smla_sparse_decode_noalloc: these sizes need %zu bytes of split scratch, more than its fixed %zu; "
+                "use smla_sparse_decode with a workspace",
+                need, dec::kNoAllocScratchBytes);
+  *out = nullptr;
+  if (need == 0) return SMLA_OK;
+  return noalloc_scratch(out);
 }
 
 }  // namespace smla

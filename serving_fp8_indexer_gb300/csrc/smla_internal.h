@@ -63,6 +63,11 @@ smla_status_t launch_attention(const AttnArgs& a, unsigned* err, cudaStream_t st
 // and the kernel that combines the partials into the bf16 output.
 int decode_splits(int T, int H, int indices_stride);
 size_t decode_workspace_bytes(int T, int H, int nsplit);
+// Fixed scratch of smla_sparse_decode_noalloc (a static device array): its
+// size, and its device address on the current device when `need` bytes fit
+// (SMLA_ERR_UNSUPPORTED otherwise; nullptr when need is 0).
+size_t noalloc_scratch_bytes();
+smla_status_t noalloc_scratch_for(size_t need, void** out);
 smla_status_t launch_decode_combine(const float* part_o, const float* part_lse, const float* sink, int T, int H,
                                     int nsplit, uint16_t* out, cudaStream_t stream);
 
