@@ -143,6 +143,22 @@ smla_status_t smla_sparse_prefill(const void* q, int32_t q_dtype, const uint8_t*
                                   int32_t v_depth, float softmax_scale, const float* attn_sink,
                                   uint16_t* out, cudaStream_t stream);
 
+/* Sparse MLA prefill over a BF16 latent cache: "mla_sm100_prefill_sparse_fp8"
+ * names itself the FP8 KV-cache variant of "mla_sm100_prefill_sparse"; this
+ * is that BF16-cache form.  The same computation as smla_sparse_prefill with
+ * K_j = latent_pool[indices[t,j]] read as bf16 (no scales):
+ *   q            bf16 [T, H, 576]
+ *   latent_pool  bf16 [phys_rows, 576] (512 nope + 64 rope)
+ *   indices, topk_lengths, attn_sink, out, H, v_depth: as smla_sparse_prefill
+ * Alignment: q, latent_pool and out 16 bytes; indices, topk_lengths and
+ * attn_sink 4 bytes.  The products run as tcgen05 kind::f16 (bf16 x bf16)
+ * MMAs with f32 TMEM accumulation; P is rounded to bf16. */
+smla_status_t smla_sparse_prefill_bf16_cache(const uint16_t* q, const uint16_t* latent_pool, int64_t phys_rows,
+                                             const uint32_t* indices, int32_t indices_stride,
+                                             const uint32_t* topk_lengths, int32_t T, int32_t H,
+                                             int32_t v_depth, float softmax_scale, const float* attn_sink,
+                                             uint16_t* out, cudaStream_t stream);
+
 /* Dense causal MLA prefill over the paged latent cache, for prompts short
  * enough that a top-k selection would keep every key.  "SM100MLA" (the
  * dense MLA prefill struct page) and "mla_sm100_prefill_blockscale" (dense

@@ -167,8 +167,13 @@ def topk(scores, k, cu_q, kv_len, page_table, page_size, tokens=None):
 def dequant_rows(latent, scales, scale_block_size, rows, qk_depth=576):
     """Dequantised latent rows, float64 [len(rows), qk_depth]:
     e4m3(byte) * scale(row, d) with scale = 1 (sbs == 0), scales[row, 0]
-    (sbs >= qk_depth), or scales[row, d // sbs] (0 < sbs < qk_depth)."""
+    (sbs >= qk_depth), or scales[row, d // sbs] (0 < sbs < qk_depth).  A
+    uint16 latent is a BF16 cache (the mla_sm100_prefill_sparse form the
+    FP8 page names as its base), read exactly and unscaled."""
     rows = np.asarray(rows, dtype=np.int64)
+    if np.asarray(latent).dtype == np.uint16:
+        assert int(scale_block_size) == 0, "a bf16 cache carries no scales"
+        return decode_bf16(latent[rows])
     x = decode_e4m3(latent[rows])
     sbs = int(scale_block_size)
     if sbs == 0:

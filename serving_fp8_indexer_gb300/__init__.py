@@ -13,6 +13,7 @@ from ._lib import (  # noqa: F401
     topk_workspace_size,
     topk,
     sparse_prefill,
+    sparse_prefill_bf16_cache,
     dense_prefill,
     sparse_decode_workspace_size,
     sparse_decode,

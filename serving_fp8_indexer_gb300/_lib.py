@@ -25,7 +25,7 @@ SMLA_BF16 = 0
 SMLA_E4M3 = 1
 
 EXPORTED = ("smla_indexer_scores", "smla_topk_workspace_size", "smla_topk", "smla_sparse_prefill",
-            "smla_dense_prefill", "smla_sparse_decode_workspace_size", "smla_sparse_decode",
+            "smla_sparse_prefill_bf16_cache", "smla_dense_prefill", "smla_sparse_decode_workspace_size", "smla_sparse_decode",
             "smla_sparse_decode_noalloc",
             "smla_check_device_errors", "smla_selftest_wait_timeout", "smla_last_error", "smla_version")
 
@@ -64,6 +64,7 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.smla_topk_workspace_size.restype = sz
         lib.smla_topk.argtypes = [vp, i64, SeqsT, i32, vp, vp, vp, sz, vp]
         lib.smla_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
+        lib.smla_sparse_prefill_bf16_cache.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i32, f32, vp, vp, vp]
         lib.smla_dense_prefill.argtypes = [vp, i32, vp, i64, vp, i32, SeqsT, i32, i32, f32, vp, vp, vp]
         lib.smla_sparse_decode_workspace_size.argtypes = [i32, i32, i32]
         lib.smla_sparse_decode_workspace_size.restype = sz
@@ -76,7 +77,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.smla_last_error.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
         lib.smla_last_error.restype = ctypes.c_size_t
         lib.smla_version.restype = ctypes.c_char_p
-        for name in ("smla_indexer_scores", "smla_topk", "smla_sparse_prefill", "smla_dense_prefill",
+        for name in ("smla_indexer_scores", "smla_topk", "smla_sparse_prefill", "smla_sparse_prefill_bf16_cache",
+                     "smla_dense_prefill",
                      "smla_sparse_decode", "smla_sparse_decode_noalloc", "smla_check_device_errors",
                      "smla_selftest_wait_timeout"):
             getattr(lib, name).restype = ctypes.c_int
@@ -199,6 +201,23 @@ def sparse_prefill(q: torch.Tensor, latent: torch.Tensor, scales: Optional[torch
                                  _ptr(topk_lengths, torch.uint32, "topk_lengths", 1), T, H, int(out.shape[2]),
                                  float(softmax_scale), _ptr(attn_sink, torch.float32, "attn_sink", 1),
                                  _ptr(out, torch.bfloat16, "out", 3), _stream(stream))
+    _check(lib, st)
+    return out
+
+
+def sparse_prefill_bf16_cache(q: torch.Tensor, latent: torch.Tensor, indices: torch.Tensor,
+                              topk_lengths: torch.Tensor, softmax_scale: float, out: torch.Tensor,
+                              attn_sink: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Sparse MLA prefill over a BF16 latent cache: q bf16 [T, H, 576], latent
+    bf16 [phys_rows, 576]; the other arguments as sparse_prefill."""
+    lib = load()
+    T, H = int(q.shape[0]), int(q.shape[1])
+    st = lib.smla_sparse_prefill_bf16_cache(_ptr(q, torch.bfloat16, "q", 3), _ptr(latent, torch.bfloat16, "latent", 2),
+                                            int(latent.shape[0]), _ptr(indices, torch.uint32, "indices", 2),
+                                            int(indices.shape[1]), _ptr(topk_lengths, torch.uint32, "topk_lengths", 1),
+                                            T, H, int(out.shape[2]), float(softmax_scale),
+                                            _ptr(attn_sink, torch.float32, "attn_sink", 1),
+                                            _ptr(out, torch.bfloat16, "out", 3), _stream(stream))
     _check(lib, st)
     return out
 

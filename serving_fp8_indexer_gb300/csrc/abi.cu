@@ -268,6 +268,23 @@ smla_status_t smla_sparse_prefill(const void* q, int32_t q_dtype, const uint8_t*
   return launch_attention(a, err, stream);
 }
 
+smla_status_t smla_sparse_prefill_bf16_cache(const uint16_t* q, const uint16_t* latent_pool, int64_t phys_rows,
+                                             const uint32_t* indices, int32_t indices_stride,
+                                             const uint32_t* topk_lengths, int32_t T, int32_t H, int32_t v_depth,
+                                             float softmax_scale, const float* attn_sink, uint16_t* out,
+                                             cudaStream_t stream) {
+  g_last_error.clear();
+  smla_status_t st = check_attn(q, SMLA_BF16, latent_pool, phys_rows, nullptr, 0, true, indices, indices_stride,
+                                topk_lengths, T, H, v_depth, softmax_scale, attn_sink, out);
+  if (st != SMLA_OK || T == 0) return st;
+  unsigned* err = nullptr;
+  st = device_err_ptr(&err);
+  if (st != SMLA_OK) return st;
+  AttnArgs a{q, SMLA_BF16, reinterpret_cast<const uint8_t*>(latent_pool), phys_rows, nullptr, 0, indices,
+             indices_stride, topk_lengths, nullptr, T, H, softmax_scale, attn_sink, out, 1, nullptr, nullptr, 1};
+  return launch_attention(a, err, stream);
+}
+
 smla_status_t smla_dense_prefill(const void* q, int32_t q_dtype, const uint8_t* latent_pool, int64_t phys_rows,
                                  const float* scales, int32_t scale_block_size, smla_seqs_t seqs, int32_t H,
                                  int32_t v_depth, float softmax_scale, const float* attn_sink, uint16_t* out,

@@ -150,12 +150,15 @@ struct Params {
   float* part_lse;
 };
 
-template <int QP, int KVP, int PP, int NST>
+// EB: bytes per latent element in the cache: 1 (e4m3) or 2 (bf16 cache;
+// then q is bf16, one term, and QK / PV run as kind::f16 bf16 MMAs).
+template <int QP, int KVP, int PP, int NST, int EB = 1>
 struct Smem {
   // Q as the QK B operand, [chunk][QP x 64 rows][64 B]: for bf16 q the hi
-  // rows 0..63 and lo rows 64..127 of a chunk are one 128-row operand
-  uint8_t q[QP * kQBytes];
-  uint8_t kv[NST][KVP][kKVBytes];
+  // rows 0..63 and lo rows 64..127 of a chunk are one 128-row operand; with
+  // a bf16 cache, 18 chunks of 64 rows
+  uint8_t q[QP * EB * kQBytes];
+  uint8_t kv[NST][KVP][EB * kKVBytes];
   uint8_t plo[PP == 2 ? kChunkBytes : 16];  // P lo term (bf16 path)
   uint32_t idx[kBK];
   float srow[NST][kBK];  // per-row scale (1 for unit)
@@ -286,20 +289,23 @@ __device__ __forceinline__ void split_quarter(uint8_t* hi_buf, uint8_t* lo_buf, 
 // each key tile is read once for both), the MMAs rotating over NACC
 // accumulators (MMA i of the block goes to accumulator i % NACC; the first
 // NACC overwrite).  Every operand offset is a compile-time constant.
-template <int QP, int KVP, int NACC>
+template <int QP, int KVP, int NACC, int EB>
 __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t a0, uint64_t b0, uint32_t idesc) {
   constexpr int kQN = QP * kNH;
 #pragma unroll
-  for (int kc = 0; kc < kChunks; ++kc)
+  for (int kc = 0; kc < kChunks * EB; ++kc)
 #pragma unroll
-    for (int kk = 0; kk < 2; ++kk)
+    for (int kk = 0; kk < 2; ++kk)  // two 32-byte K steps per 64-byte chunk
 #pragma unroll
       for (int kp = 0; kp < KVP; ++kp) {
         const int i = (kc * 2 + kk) * KVP + kp;
         // descriptor address fields are in 16-byte units: add offsets >> 4
-        const uint64_t ad = a0 + static_cast<uint64_t>((kp * kKVBytes + kc * kChunkBytes + kk * 32) >> 4);
+        const uint64_t ad = a0 + static_cast<uint64_t>((kp * EB * kKVBytes + kc * kChunkBytes + kk * 32) >> 4);
         const uint64_t bd = b0 + static_cast<uint64_t>((kc * kQN * 64 + kk * 32) >> 4);
-        mma_f8f6f4_ss(s_tmem + (i % NACC) * kQN, ad, bd, idesc, i < NACC ? 0u : 1u);
+        if (EB == 2)
+          mma_f16_ss(s_tmem + (i % NACC) * kQN, ad, bd, idesc, i < NACC ? 0u : 1u);
+        else
+          mma_f8f6f4_ss(s_tmem + (i % NACC) * kQN, ad, bd, idesc, i < NACC ? 0u : 1u);
       }
 }
 
@@ -376,10 +382,15 @@ __device__ __forceinline__ Item item_at(const Params& p, int w, int groups) {
 // phases come from its index g over all of this CTA's blocks), so the next
 // item's first rows are gathered, and its q split, while the current item's
 // last blocks and epilogue run.
-template <int QP, int KVP, int PP, int NST, int SC, int KEYS>
+template <int QP, int KVP, int PP, int NST, int SC, int KEYS, int EB>
 __global__ void __launch_bounds__(threads_for(KVP), 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tq, const Params p) {
-  using S = Smem<QP, KVP, PP, NST>;
+  using S = Smem<QP, KVP, PP, NST, EB>;
+  static_assert(EB == 1 || (QP == 1 && KVP == 1 && PP == 1 && SC == kUnit),
+                "a bf16 cache takes bf16 q as one term, single-term P and no scales");
+  constexpr int kCh = kChunks * EB;       // 64-byte chunks per cache row
+  constexpr int kSlotBytes = EB * kKVBytes;
+  constexpr int kRopeCh = kRope * EB;     // chunk of column 512 (P goes there)
   static_assert(!(PP == 2 && KVP == 2), "P lo has a buffer only when rows are single-term");
   static_assert(KVP == 1 || NST == 1, "the blockwise quarter barriers complete once per block (one slot)");
   static_assert(offsetof(S, kv) % 1024 == 0 && offsetof(S, plo) % 1024 == 0,
@@ -515,7 +526,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
       } else {
         // e4m3 q is in place; rows past the item's heads (another token's) are zeroed
         if (I.hv < kNH)
-          for (int i = threadIdx.x; i < kChunks * kNH * 4; i += kSoftThreads) {
+          for (int i = threadIdx.x; i < kCh * kNH * 4; i += kSoftThreads) {
             const int row = (i >> 2) % kNH;
             if (row >= I.hv) *reinterpret_cast<uint4*>(&s.q[(i >> 2) * 64 + (i & 3) * 16]) = make_uint4(0, 0, 0, 0);
           }
@@ -690,7 +701,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         }
         // ---- P row r (this thread's 32 heads) and the row sums
         const float isr = 1.f / sr;
-        uint8_t* p_hi = &s.kv[slot][0][kRope * kChunkBytes];
+        uint8_t* p_hi = &s.kv[slot][0][kRopeCh * kChunkBytes];
         uint4 lo_keep[2];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -702,7 +713,19 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
             lv[h] = SC == kUnit ? lv[h] + x[k] : fmaf(x[k], isr, lv[h]);
           }
           const int c4 = half * 2 + c;
-          if (PP == 2) {
+          if (EB == 2) {
+            // bf16 P: heads hb .. hb+31 fill chunk kRopeCh + half, 16 heads
+            // (two 16-byte pieces) per c
+            uint32_t w[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(x[2 * k], x[2 * k + 1]);
+              w[k] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            uint8_t* prow = p_hi + half * kChunkBytes + r * 64;
+            *reinterpret_cast<uint4*>(prow + sw64(r, 2 * c)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(prow + sw64(r, 2 * c + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+          } else if (PP == 2) {
             uint4 hi;
             split16(x, hi, lo_keep[c]);
             *reinterpret_cast<uint4*>(p_hi + r * 64 + sw64(r, c4)) = hi;
@@ -822,13 +845,13 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     // one elected lane issues.
     setmaxnreg_dec<kLowRegs>();
     const bool leader = elect_one();
-    constexpr uint32_t IDESC_QK = idesc_e4m3_f32(kBK, kQN, 0, 0);
+    constexpr uint32_t IDESC_QK = EB == 2 ? idesc_bf16_f32(kBK, kQN, 0, 0) : idesc_e4m3_f32(kBK, kQN, 0, 0);
     const uint64_t qk_b0 = make_sdesc(smem_u32(s.q), 16, 512, kSwizzle64B);
     const uint64_t kv_a0 = make_sdesc(smem_u32(s.kv[0][0]), 16, 512, kSwizzle64B);
     // q of the CTA's next item with keys, requested once the last QK of the
     // item before it has completed (s.q is then free).  With a 3-D tensor
     // map one load brings all column boxes, else one load per box.
-    constexpr int kQBoxes = QP == 2 ? 2 * kChunks : kChunks;
+    constexpr int kQBoxes = QP == 2 ? 2 * kChunks : kCh;
     const uint64_t q_policy = make_policy_evict_first();  // q is read once
     int q_issued = 0;
     auto issue_q = [&](int w) {
@@ -870,9 +893,9 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
                                   : mbar_wait(smem_u32(&s.bar_kv_full[g % NST]), (g / NST) & 1, p.err));
         if (!__all_sync(0xffffffffu, wt)) { ok = false; break; }
         tc_fence_after();  // after the softmax's tcgen05.ld of S
-        const uint64_t slot_off = static_cast<uint64_t>(((g % NST) * KVP * kKVBytes) >> 4);
+        const uint64_t slot_off = static_cast<uint64_t>(((g % NST) * KVP * kSlotBytes) >> 4);
         if (leader) {
-          issue_qk<QP, KVP, kSAcc>(tmem + kTmemS, kv_a0 + slot_off, qk_b0, IDESC_QK);
+          issue_qk<QP, KVP, kSAcc, EB>(tmem + kTmemS, kv_a0 + slot_off, qk_b0, IDESC_QK);
           mma_commit(smem_u32(&s.bar_s_full));
         }
         __syncwarp();
@@ -897,7 +920,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     // barrier) and, after a rescale, rescaled all lanes (a barrier).
     setmaxnreg_dec<kLowRegs>();
     const bool leader = elect_one();
-    constexpr uint32_t IDESC_PV = idesc_e4m3_f32(128, kNH, 1, 1);
+    constexpr uint32_t IDESC_PV = EB == 2 ? idesc_bf16_f32(128, kNH, 1, 1) : idesc_e4m3_f32(128, kNH, 1, 1);
     const uint64_t pv_a0 = make_sdesc(smem_u32(s.kv[0][0]), kChunkBytes, 512, kSwizzle64B);
     const uint64_t plo0 = make_sdesc(smem_u32(s.plo), kChunkBytes, 512, kSwizzle64B);
     int gb = 0;
@@ -912,7 +935,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         // back to the gather when its MMAs complete.  P hi sits in the slot's
         // rope chunk, P lo in its own buffer.
         const int slot = g % NST;
-        const uint64_t slot_off = static_cast<uint64_t>((slot * KVP * kKVBytes) >> 4);
+        const uint64_t slot_off = static_cast<uint64_t>((slot * KVP * kSlotBytes) >> 4);
 #pragma unroll
         for (int ks = 0; ks < kRowQ; ++ks) {
           if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_p_full[ks]), g & 1, p.err))) {
@@ -926,14 +949,21 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
 #pragma unroll
               for (int kp = 0; kp < KVP; ++kp)
 #pragma unroll
-                for (int tile = 0; tile < 4; ++tile) {
-                  const uint32_t pacc = (j > 0 || pp > 0 || kp > 0 || ks > 0) ? 1u : 0u;
-                  const uint64_t ad = pv_a0 + slot_off +
-                                      static_cast<uint64_t>((kp * kKVBytes + (2 * tile) * kChunkBytes + ks * 32 * 64) >> 4);
-                  const uint64_t bd = pp == 0 ? pv_a0 + slot_off + static_cast<uint64_t>((kRope * kChunkBytes + ks * 32 * 64) >> 4)
-                                              : plo0 + static_cast<uint64_t>((ks * 32 * 64) >> 4);
-                  mma_f8f6f4_ss(tmem + tile * kNH, ad, bd, IDESC_PV, pacc);
-                }
+                for (int tile = 0; tile < 4; ++tile)
+#pragma unroll
+                  for (int kst = 0; kst < EB; ++kst) {  // K steps of 32 (e4m3) or 16 (bf16) keys
+                    const uint32_t pacc = (j > 0 || pp > 0 || kp > 0 || ks > 0 || kst > 0) ? 1u : 0u;
+                    // value tile: 128 columns = 2 * EB chunks; key rows 32 ks + 16 kst (bf16)
+                    const int krow = ks * 32 + kst * 16;
+                    const uint64_t ad = pv_a0 + slot_off +
+                                        static_cast<uint64_t>((kp * kSlotBytes + (2 * EB * tile) * kChunkBytes + krow * 64) >> 4);
+                    const uint64_t bd = pp == 0 ? pv_a0 + slot_off + static_cast<uint64_t>((kRopeCh * kChunkBytes + krow * 64) >> 4)
+                                                : plo0 + static_cast<uint64_t>((ks * 32 * 64) >> 4);
+                    if (EB == 2)
+                      mma_f16_ss(tmem + tile * kNH, ad, bd, IDESC_PV, pacc);
+                    else
+                      mma_f8f6f4_ss(tmem + tile * kNH, ad, bd, IDESC_PV, pacc);
+                  }
             mma_commit(smem_u32(&s.bar_kv_empty[slot][ks]));
           }
           __syncwarp();
@@ -1030,11 +1060,12 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         for (int q = 0; q < kRowQ; ++q) {
           if (q > 0 && ok) ok = mbar_wait(smem_u32(&s.bar_kv_empty[slot][q]), par, p.err);
           if (ok) {
+            constexpr int kPieces = 36 * EB;  // 16-byte pieces of a cache row
 #pragma unroll 2
-            for (int i = pt; i < 32 * 36; i += kProdThreads) {
-              const int row = 32 * q + i / 36, c = i % 36;
+            for (int i = pt; i < 32 * kPieces; i += kProdThreads) {
+              const int row = 32 * q + i / kPieces, c = i % kPieces;
               const uint32_t dst = smem_u32(s.kv[slot][0]) + (c >> 2) * kChunkBytes + row * 64 + sw64(row, c & 3);
-              cp_async16_hint(dst, p.latent + static_cast<int64_t>(s.idx[row]) * kD + c * 16, keep);
+              cp_async16_hint(dst, p.latent + static_cast<int64_t>(s.idx[row]) * (kD * EB) + c * 16, keep);
             }
             if (KVP == 2 && pt < 32) {
               const int row = 32 * q + pt;
@@ -1076,17 +1107,17 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-template <int QP, int KVP, int PP, int NST, int SC, int KEYS>
+template <int QP, int KVP, int PP, int NST, int SC, int KEYS, int EB = 1>
 static smla_status_t launch_k(const CUtensorMap& tq, const Params& p, cudaStream_t stream) {
-  const size_t smem = sizeof(Smem<QP, KVP, PP, NST>);
-  static_assert(sizeof(Smem<QP, KVP, PP, NST>) <= 232448, "the variant's shared memory exceeds a CTA's 227 KB");
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<QP, KVP, PP, NST, SC, KEYS>,
+  const size_t smem = sizeof(Smem<QP, KVP, PP, NST, EB>);
+  static_assert(sizeof(Smem<QP, KVP, PP, NST, EB>) <= 232448, "the variant's shared memory exceeds a CTA's 227 KB");
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<QP, KVP, PP, NST, SC, KEYS, EB>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return fail_cuda(e, "prefill smem attribute");
   // The register split (setmaxnreg) draws on the launch allocation: refuse a
   // build whose register count would leave the softmax's increase waiting.
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, prefill_kernel<QP, KVP, PP, NST, SC, KEYS>);
+  e = cudaFuncGetAttributes(&fa, prefill_kernel<QP, KVP, PP, NST, SC, KEYS, EB>);
   if (e != cudaSuccess) return fail_cuda(e, "prefill attributes");
   if (fa.numRegs != kLaunchRegs)
     return fail(SMLA_ERR_UNSUPPORTED, "prefill kernel built with %d registers a thread, the register split needs %d",
@@ -1094,7 +1125,7 @@ static smla_status_t launch_k(const CUtensorMap& tq, const Params& p, cudaStream
   // persistent: one CTA per SM (shared memory allows no more), at most one per item
   const int64_t items = static_cast<int64_t>(p.T) * ((p.H + kNH - 1) / kNH) * p.nsplit;
   const dim3 grid(static_cast<unsigned>(std::min<int64_t>(items, device_sm_count())));
-  prefill_kernel<QP, KVP, PP, NST, SC, KEYS><<<grid, threads_for(KVP), smem, stream>>>(tq, p);
+  prefill_kernel<QP, KVP, PP, NST, SC, KEYS, EB><<<grid, threads_for(KVP), smem, stream>>>(tq, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return fail_cuda(e, "prefill launch");
   return SMLA_OK;
@@ -1158,6 +1189,13 @@ smla_status_t launch_attention(const AttnArgs& a, unsigned* err, cudaStream_t st
   }
   if (!p.q_box3d && !encode_tma_2d_u8(&tq, a.q, pitch, static_cast<uint64_t>(T) * H, 64, kNH, 64))
     return fail(SMLA_ERR_CUDA, "cuTensorMapEncodeTiled failed for the prefill q tensor map");
+  if (a.cache_bf16) {
+    // bf16 cache: bf16 x bf16 MMAs, one gather slot (a 128-row block of
+    // 1152-byte rows and the 64-head bf16 q fill shared memory)
+    if (!bf16 || sbs != 0 || p.keys != kIndexed)
+      return fail(SMLA_ERR_UNSUPPORTED, "a bf16 cache takes bf16 q, no scales and indexed keys");
+    return launch_k<1, 1, 1, 1, kUnit, kIndexed, 2>(tq, p, stream);
+  }
   if (sbs == 0) return bf16 ? launch_t<2, 1, 2, 2, kUnit>(tq, p, stream) : launch_t<1, 1, 1, 2, kUnit>(tq, p, stream);
   if (sbs >= kD) return bf16 ? launch_t<2, 1, 2, 2, kRow>(tq, p, stream) : launch_t<1, 1, 1, 2, kRow>(tq, p, stream);
   return launch_t<1, 2, 1, 1, kBlock>(tq, p, stream);

@@ -214,6 +214,15 @@ SMLA_DEVICE_INLINE void mma_f8f6f4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (here bf16 x bf16), issued by one thread.
+SMLA_DEVICE_INLINE void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrives (once) on `bar` when every tcgen05 op issued so far by this thread completes.
 SMLA_DEVICE_INLINE void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -275,6 +284,16 @@ SMLA_DEVICE_INLINE uint64_t make_sdesc(uint32_t saddr, uint32_t lbo_bytes, uint3
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, int a_mn, int b_mn) {
   return (1u << 4)                                   // D = f32
          | (0u << 7) | (0u << 10)                    // A, B = e4m3
+         | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16)
+         | (static_cast<uint32_t>(N >> 3) << 17)
+         | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor for kind::f16 with bf16 A and B, f32 accumulator
+// (same field layout as above; A / B format 1 = bf16).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4)                                   // D = f32
+         | (1u << 7) | (1u << 10)                    // A, B = bf16
          | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16)
          | (static_cast<uint32_t>(N >> 3) << 17)
          | (static_cast<uint32_t>(M >> 4) << 24);

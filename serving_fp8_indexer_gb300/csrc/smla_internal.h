@@ -56,6 +56,7 @@ struct AttnArgs {
   int nsplit;
   float* part_o;    // [T, nsplit, H, 512]
   float* part_lse;  // [T, nsplit, H]
+  int cache_bf16;   // latent_pool holds bf16 [phys_rows, 576] (q bf16, no scales)
 };
 smla_status_t launch_attention(const AttnArgs& a, unsigned* err, cudaStream_t stream);
 

@@ -154,7 +154,7 @@ class Workload:
     H: int = 0
     q_dtype: int = Q_BF16
     q_attn: Optional[np.ndarray] = None      # uint16 bf16 bits or uint8 e4m3, [T, H, 576]
-    latent: Optional[np.ndarray] = None      # uint8 [phys_rows, 576]
+    latent: Optional[np.ndarray] = None      # uint8 e4m3 [phys_rows, 576] (uint16 bf16 for a BF16 cache)
     scale_block_size: int = 0
     scales: Optional[np.ndarray] = None      # f32 [phys_rows, ceil(576/sbs)] or None
     indices: Optional[np.ndarray] = None     # uint32 [T, topk] physical rows (sampled workloads)
@@ -197,7 +197,7 @@ def sample_causal_indices(rng, seqs: Seqs, k: int):
 
 
 def build(name: str, seed: int, q_lens, kv_lens, page_size=64, *, h_idx=0, topk=0,
-          H=0, q_dtype=Q_BF16, sbs=0, sample_indices=False) -> Workload:
+          H=0, q_dtype=Q_BF16, sbs=0, sample_indices=False, latent_bf16=False) -> Workload:
     rng = np.random.default_rng(seed)
     seqs = make_seqs(rng, q_lens, kv_lens, page_size)
     T, R = seqs.T, seqs.phys_rows
@@ -209,7 +209,11 @@ def build(name: str, seed: int, q_lens, kv_lens, page_size=64, *, h_idx=0, topk=
         w.k_pool = _normal_e4m3(rng, (R, IDX_DEPTH))
         w.k_scale = rng.uniform(0.5, 1.5, size=(R,)).astype(np.float32)
     if H:
-        w.latent, w.scales = _quantise_latent(rng, R, sbs)
+        if latent_bf16:  # a BF16 latent cache (no scales): N(0,1) rounded to bf16
+            assert sbs == 0
+            w.latent, w.scales = _normal_bf16(rng, (R, QK_DEPTH)), None
+        else:
+            w.latent, w.scales = _quantise_latent(rng, R, sbs)
         if q_dtype == Q_BF16:
             w.q_attn = _normal_bf16(rng, (T, H, QK_DEPTH))
         else:

@@ -23,7 +23,7 @@ def lib():
 def declared_entry_points():
     src = open(os.path.join(ROOT, "include", "smla.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(smla_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(smla_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_exports_every_declared_symbol(lib):

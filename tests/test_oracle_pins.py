@@ -430,3 +430,34 @@ def test_dense_prefill_equals_causal_sdpa_over_pages():
             Q[None], K[None, None].expand(1, H, L, 576), K[None, None, :, :512].expand(1, H, L, 512),
             attn_mask=mask, scale=sc)[0].permute(1, 0, 2).numpy()
         assert np.allclose(out[a:e], ref, rtol=1e-11, atol=1e-13)
+
+
+def test_bf16_cache_reads_exactly():
+    """A BF16 cache is read as its exact values: rows holding e4m3-exact
+    values give the e4m3 cache's result bit for bit, and k = every causal
+    key matches float64 scaled_dot_product_attention with K, V from torch's
+    bfloat16."""
+    rng = np.random.default_rng(35)
+    latent, q, idx = _attn_inputs(rng, 3, 4, 60, 20)
+    lat16 = torch.from_numpy(latent).view(torch.float8_e4m3fn).to(torch.bfloat16).view(torch.int16).numpy()
+    lat16 = lat16.view(np.uint16)
+    lens = np.array([20, 5, 1], np.uint32)
+    a = oracle.sparse_prefill(q, 0, latent, None, 0, idx, lens, 0.06)
+    b = oracle.sparse_prefill(q, 0, lat16, None, 0, idx, lens, 0.06)
+    assert np.array_equal(a, b)
+    L, H = 23, 2
+    seqs = wl.make_seqs(rng, [L], [L], 8)
+    lat = wl.to_bf16_bits(rng.standard_normal((seqs.phys_rows, 576)).astype(np.float32))
+    qq = wl.to_bf16_bits(rng.standard_normal((L, H, 576)).astype(np.float32))
+    rows = wl.logical_to_phys(seqs, 0, np.arange(L))
+    ind = np.full((L, L), 0xFFFFFFFF, np.uint32)
+    for t in range(L):
+        ind[t, :t + 1] = rows[:t + 1]
+    sc = 1 / math.sqrt(576)
+    out = oracle.sparse_prefill(qq, 0, lat, None, 0, ind, np.arange(1, L + 1, dtype=np.uint32), sc)
+    K = torch.from_numpy(lat[rows].view(np.int16)).view(torch.bfloat16).double()
+    Q = torch.from_numpy(qq.view(np.int16)).view(torch.bfloat16).double().permute(1, 0, 2)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        Q[None], K[None, None].expand(1, H, L, 576), K[None, None, :, :512].expand(1, H, L, 512),
+        is_causal=True, scale=sc)[0].permute(1, 0, 2).numpy()
+    assert np.allclose(out, ref, rtol=1e-11, atol=1e-13)
