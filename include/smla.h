@@ -107,6 +107,32 @@ smla_status_t smla_topk(const float* scores, int64_t score_stride, smla_seqs_t s
                         uint32_t* indices, uint32_t* topk_lengths, void* workspace, size_t workspace_bytes,
                         cudaStream_t stream);
 
+/* Stages 1 + 2 fused -- indexer scores and per-token top-k in one pass, the
+ * score rows kept in the SM's shared memory instead of an HBM buffer.
+ * "sparse_index_fp8_sm100" (module summary: the scorer is a drop-in for the
+ * buffer the top-k stage reads, and the fusions that follow it are left to
+ * later work).  Outputs exactly what smla_indexer_scores followed by
+ * smla_topk produce: the same scores (same MMAs and epilogue arithmetic in
+ * the same order), the same selection rule (ties to the lower logical key),
+ * indices u32 [T, k] in ascending logical-key order with the 0xFFFFFFFF
+ * tail, topk_lengths u32 [T].
+ *   q, q_scale, k_pool, k_scale, phys_rows, seqs, H_idx: as smla_indexer_scores
+ *   score_stride: a bound on every kv_len (>= max kv_len, multiple of 4), as
+ *                 the unfused pair's score row stride
+ *   k, indices, topk_lengths: as smla_topk
+ * Rows of up to 128 * H_idx keys (8192 at H_idx 64) stay on chip and need no
+ * workspace; for a larger score_stride the call runs the unfused pair with
+ * the score buffer [T, score_stride] in `workspace`.  workspace: caller-owned
+ * device scratch of at least smla_indexer_topk_workspace_size(T,
+ * score_stride, H_idx, k) bytes (16-byte aligned; NULL when that is 0);
+ * contents on entry do not matter, unspecified on return.  Errors and
+ * alignment as for the two stages. */
+size_t smla_indexer_topk_workspace_size(int32_t T, int64_t score_stride, int32_t H_idx, int32_t k);
+smla_status_t smla_indexer_topk(const uint8_t* q, const float* q_scale, const uint8_t* k_pool,
+                                const float* k_scale, int64_t phys_rows, smla_seqs_t seqs, int32_t H_idx,
+                                int64_t score_stride, int32_t k, uint32_t* indices, uint32_t* topk_lengths,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Stage 3 -- sparse MLA prefill attention.
  * "mla_sm100_prefill_sparse_fp8" (Modular Mojo function page: arguments,
  * scale_block_size modes) and "mla_prefill_sparse_qkv_fp8" (K and V share

@@ -12,6 +12,8 @@ from ._lib import (  # noqa: F401
     indexer_scores,
     topk_workspace_size,
     topk,
+    indexer_topk_workspace_size,
+    indexer_topk,
     sparse_prefill,
     sparse_prefill_bf16_cache,
     dense_prefill,

@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTE
 SMLA_BF16 = 0
 SMLA_E4M3 = 1
 
-EXPORTED = ("smla_indexer_scores", "smla_topk_workspace_size", "smla_topk", "smla_sparse_prefill",
+EXPORTED = ("smla_indexer_scores", "smla_topk_workspace_size", "smla_topk", "smla_indexer_topk_workspace_size",
+            "smla_indexer_topk", "smla_sparse_prefill",
             "smla_sparse_prefill_bf16_cache", "smla_dense_prefill", "smla_sparse_decode_workspace_size", "smla_sparse_decode",
             "smla_sparse_decode_noalloc",
             "smla_check_device_errors", "smla_selftest_wait_timeout", "smla_last_error", "smla_version")
@@ -64,6 +65,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.smla_topk_workspace_size.restype = sz
         lib.smla_topk.argtypes = [vp, i64, SeqsT, i32, vp, vp, vp, sz, vp]
         lib.smla_selftest_wait_timeout.argtypes = [ctypes.c_uint32, vp]
+        lib.smla_indexer_topk_workspace_size.argtypes = [i32, i64, i32, i32]
+        lib.smla_indexer_topk_workspace_size.restype = sz
+        lib.smla_indexer_topk.argtypes = [vp, vp, vp, vp, i64, SeqsT, i32, i64, i32, vp, vp, vp, sz, vp]
         lib.smla_sparse_prefill_bf16_cache.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i32, f32, vp, vp, vp]
         lib.smla_dense_prefill.argtypes = [vp, i32, vp, i64, vp, i32, SeqsT, i32, i32, f32, vp, vp, vp]
         lib.smla_sparse_decode_workspace_size.argtypes = [i32, i32, i32]
@@ -77,7 +81,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.smla_last_error.argtypes = [ctypes.c_char_p, ctypes.c_size_t]
         lib.smla_last_error.restype = ctypes.c_size_t
         lib.smla_version.restype = ctypes.c_char_p
-        for name in ("smla_indexer_scores", "smla_topk", "smla_sparse_prefill", "smla_sparse_prefill_bf16_cache",
+        for name in ("smla_indexer_scores", "smla_topk", "smla_indexer_topk", "smla_sparse_prefill",
+                     "smla_sparse_prefill_bf16_cache",
                      "smla_dense_prefill",
                      "smla_sparse_decode", "smla_sparse_decode_noalloc", "smla_check_device_errors",
                      "smla_selftest_wait_timeout"):
@@ -175,6 +180,30 @@ def topk(scores: torch.Tensor, seqs: Seqs, k: int, indices: torch.Tensor, topk_l
     st = lib.smla_topk(_ptr(scores, torch.float32, "scores", 2), int(scores.shape[1]), seqs.as_c(), int(k),
                        _ptr(indices, torch.uint32, "indices", 2), _ptr(topk_lengths, torch.uint32, "topk_lengths", 1),
                        ws, wsb, _stream(stream))
+    _check(lib, st)
+    return indices, topk_lengths
+
+
+def indexer_topk_workspace_size(T: int, score_stride: int, H_idx: int, k: int) -> int:
+    """Bytes of device scratch smla_indexer_topk needs (0 when rows stay on chip)."""
+    return int(load().smla_indexer_topk_workspace_size(int(T), int(score_stride), int(H_idx), int(k)))
+
+
+def indexer_topk(q: torch.Tensor, q_scale: torch.Tensor, k_pool: torch.Tensor, k_scale: torch.Tensor, seqs: Seqs,
+                 score_stride: int, k: int, indices: torch.Tensor, topk_lengths: torch.Tensor,
+                 workspace: Optional[torch.Tensor] = None, stream=None):
+    """Fused indexer + top-k: indices uint32 [T, k] and topk_lengths uint32 [T]
+    as indexer_scores followed by topk, without the score buffer (rows of up
+    to 128 * H_idx keys; longer ones use `workspace`)."""
+    lib = load()
+    H_idx = int(q.shape[1]) if q.dim() == 3 else 0
+    ws = _ptr(workspace, torch.uint8, "workspace") if workspace is not None else None
+    wsb = int(workspace.numel()) if workspace is not None else 0
+    st = lib.smla_indexer_topk(_ptr(q, torch.uint8, "q", 3), _ptr(q_scale, torch.float32, "q_scale", 2),
+                               _ptr(k_pool, torch.uint8, "k_pool", 2), _ptr(k_scale, torch.float32, "k_scale", 1),
+                               int(k_pool.shape[0]), seqs.as_c(), H_idx, int(score_stride), int(k),
+                               _ptr(indices, torch.uint32, "indices", 2),
+                               _ptr(topk_lengths, torch.uint32, "topk_lengths", 1), ws, wsb, _stream(stream))
     _check(lib, st)
     return indices, topk_lengths
 

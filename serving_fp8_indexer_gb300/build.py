@@ -13,7 +13,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libsmla.so")
-SOURCES = ["abi.cu", "indexer.cu", "topk.cu", "prefill.cu", "decode.cu"]
+SOURCES = ["abi.cu", "indexer.cu", "topk.cu", "indexer_topk.cu", "prefill.cu", "decode.cu"]
 HEADERS = ["ptx.cuh", "smla_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

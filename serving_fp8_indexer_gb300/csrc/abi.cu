@@ -268,6 +268,52 @@ smla_status_t smla_sparse_prefill(const void* q, int32_t q_dtype, const uint8_t*
   return launch_attention(a, err, stream);
 }
 
+size_t smla_indexer_topk_workspace_size(int32_t T, int64_t score_stride, int32_t H_idx, int32_t k) {
+  (void)k;
+  if (T <= 0 || score_stride <= 0) return 0;
+  if (score_stride <= indexer_topk_row_cap(H_idx)) return 0;  // rows stay on chip
+  // longer rows: the score buffer [T, score_stride] f32 goes to the workspace
+  return (static_cast<size_t>(T) * static_cast<size_t>(score_stride) * sizeof(float) + 255) & ~size_t(255);
+}
+
+smla_status_t smla_indexer_topk(const uint8_t* q, const float* q_scale, const uint8_t* k_pool, const float* k_scale,
+                                int64_t phys_rows, smla_seqs_t seqs, int32_t H_idx, int64_t score_stride, int32_t k,
+                                uint32_t* indices, uint32_t* topk_lengths, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream) {
+  g_last_error.clear();
+  smla_status_t st = check_seqs(seqs);
+  if (st != SMLA_OK) return st;
+  if (H_idx != 4 && H_idx != 8 && H_idx != 16 && H_idx != 32 && H_idx != 64)
+    return fail(SMLA_ERR_UNSUPPORTED, "H_idx=%d: supported 4, 8, 16, 32, 64", H_idx);
+  if (k < 1 || k > 65536) return fail(SMLA_ERR_UNSUPPORTED, "k=%d must be in [1, 65536]", k);
+  if (score_stride < 4 || (score_stride & 3))
+    return fail(SMLA_ERR_INVALID_ARG, "score_stride=%lld must be a positive multiple of 4",
+                static_cast<long long>(score_stride));
+  const size_t need = smla_indexer_topk_workspace_size(seqs.T, score_stride, H_idx, k);
+  if (workspace_bytes < need || (need && !workspace))
+    return fail(SMLA_ERR_INVALID_ARG, "workspace: %zu bytes given, %zu needed", workspace_bytes, need);
+  if (workspace && !aligned16(workspace)) return fail(SMLA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  if (seqs.T == 0) return SMLA_OK;
+  if (!q || !q_scale || !k_pool || !k_scale || !indices || !topk_lengths)
+    return fail(SMLA_ERR_INVALID_ARG, "null pointer");
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned4(q_scale) || !aligned4(k_scale) || !aligned4(indices) ||
+      !aligned4(topk_lengths))
+    return fail(SMLA_ERR_INVALID_ARG, "q and k_pool must be 16-byte aligned; scales and outputs 4-byte aligned");
+  if (phys_rows < 1 || phys_rows >= (int64_t(1) << 31))
+    return fail(SMLA_ERR_INVALID_ARG, "phys_rows=%lld out of range", static_cast<long long>(phys_rows));
+  if (static_cast<int64_t>(seqs.T) * H_idx >= (int64_t(1) << 31)) return fail(SMLA_ERR_UNSUPPORTED, "T*H_idx too large");
+  unsigned* err = nullptr;
+  st = device_err_ptr(&err);
+  if (st != SMLA_OK) return st;
+  if (need == 0)
+    return launch_indexer_topk(q, q_scale, k_pool, k_scale, phys_rows, seqs, H_idx, k, indices, topk_lengths, err,
+                               stream);
+  float* scores = static_cast<float*>(workspace);
+  st = launch_indexer(q, q_scale, k_pool, k_scale, phys_rows, seqs, H_idx, scores, score_stride, err, stream);
+  if (st != SMLA_OK) return st;
+  return launch_topk(scores, score_stride, seqs, k, indices, topk_lengths, err, stream);
+}
+
 smla_status_t smla_sparse_prefill_bf16_cache(const uint16_t* q, const uint16_t* latent_pool, int64_t phys_rows,
                                              const uint32_t* indices, int32_t indices_stride,
                                              const uint32_t* topk_lengths, int32_t T, int32_t H, int32_t v_depth,

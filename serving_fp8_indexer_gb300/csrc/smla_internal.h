@@ -31,6 +31,13 @@ smla_status_t launch_indexer(const uint8_t* q, const float* q_scale, const uint8
                              int64_t phys_rows, const smla_seqs_t& seqs, int h_idx, float* scores,
                              int64_t score_stride, unsigned* err, cudaStream_t stream);
 
+// Fused indexer + top-k (score rows in shared memory): the longest row it
+// holds for this H_idx, and its launcher (kv_len <= that cap).
+int indexer_topk_row_cap(int h_idx);
+smla_status_t launch_indexer_topk(const uint8_t* q, const float* q_scale, const uint8_t* k_pool, const float* k_scale,
+                                  int64_t phys_rows, const smla_seqs_t& seqs, int h_idx, int k, uint32_t* indices,
+                                  uint32_t* topk_lengths, unsigned* err, cudaStream_t stream);
+
 smla_status_t launch_topk(const float* scores, int64_t score_stride, const smla_seqs_t& seqs, int k,
                           uint32_t* indices, uint32_t* topk_lengths, unsigned* err, cudaStream_t stream);
 
