@@ -177,7 +177,14 @@ CASES = {
     "blockwise": ("blockwise_fp8_prefill", dict()),
     # two of its four sequences (3072 tokens), for ncu captures
     "blockwise_small": ("blockwise_fp8_prefill", dict(lens=(1024, 2048))),
+    # the other entry points: split-K decode (8 x 2 tokens over 8192 keys),
+    # dense short-prompt prefill, and the BF16-cache form of the T=4096 shape
+    "decode": ("sparse_decode", dict()),
+    "dense": ("dense_prefill", dict()),
+    "dsv32_bf16cache": ("dsv32_prefill", dict(latent_bf16=True)),
 }
+# which attention entry point a case runs (default: smla_sparse_prefill)
+CASE_ATTN = {"decode": "decode", "dense": "dense", "dsv32_bf16cache": "bf16cache"}
 
 
 def make_workload(case="chunk"):
@@ -278,7 +285,7 @@ class Case:
     """One workload resident on the device, and one step of the path over it
     through the C ABI (indexer -> top-k -> attention, the stages it has)."""
 
-    def __init__(self, name, dev):
+    def __init__(self, name, dev, fused=False):
         import numpy as np
         import torch
 
@@ -286,10 +293,14 @@ class Case:
         from serving_fp8_indexer_gb300 import workloads as wl
         self.smla, self.torch = smla, torch
         self.name = name
+        self.attn = CASE_ATTN.get(name, "sparse")
         self.w = w = make_workload(name)
         s = w.seqs
         self.T, self.H, self.k = s.T, w.H, w.topk
         self.has_idx, self.has_attn = w.h_idx > 0, w.H > 0
+        # indexer + top-k through the fused entry point (rows on chip)
+        self.fused = fused and self.has_idx
+        self.ws = None  # split-K decode workspace
         self.stride = int(s.kv_len.max() + 3) // 4 * 4
         self.pos = wl.token_positions(s)
         self.kt = float((self.pos + 1).sum())
@@ -309,6 +320,11 @@ class Case:
             self.lens = torch.from_numpy(w.topk_lengths).to(dev) if w.topk_lengths is not None else None
         if self.has_attn:
             self.latent = torch.from_numpy(w.latent).to(dev)
+            if self.attn == "bf16cache":
+                self.latent = self.latent.view(torch.bfloat16)
+            if self.attn == "decode":
+                n = smla.sparse_decode_workspace_size(self.T, self.H, w.indices.shape[1])
+                self.ws = torch.empty(n, dtype=torch.uint8, device=dev) if n else None
             self.scales = None if w.scales is None else torch.from_numpy(w.scales).to(dev)
             if w.q_dtype == wl.Q_BF16:
                 self.t_in["q_attn"] = torch.from_numpy(w.q_attn.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -316,9 +332,13 @@ class Case:
                 self.t_in["q_attn"] = torch.from_numpy(w.q_attn).to(dev)
             self.out = torch.empty((self.T, self.H, 512), dtype=torch.bfloat16, device=dev)
         self.stream = torch.cuda.current_stream(dev)
-        self.n_kernels = (2 if self.has_idx else 0) + (1 if self.has_attn else 0)
-        attn_len = np.minimum(self.pos + 1, self.k) if self.has_idx else (
-            w.topk_lengths.astype(np.int64) if self.has_attn else np.zeros(0))
+        self.n_kernels = ((1 if self.fused else 2) if self.has_idx else 0) + (
+            (2 if self.ws is not None else 1) if self.has_attn else 0)
+        if self.attn == "dense":
+            attn_len = self.pos + 1
+        else:
+            attn_len = np.minimum(self.pos + 1, self.k) if self.has_idx else (
+                w.topk_lengths.astype(np.int64) if self.has_attn else np.zeros(0))
         self.flops = sparse_flops(attn_len, self.H) if self.has_attn else 0.0
 
     def step(self, ev=None, tin=None, o=None):
@@ -331,7 +351,13 @@ class Case:
         o_out = o if (o is not None and self.has_attn) else (self.out if self.has_attn else None)
         if ev is not None:
             ev[0].record(self.stream)
-        if self.has_idx:
+        if self.fused:
+            smla.indexer_topk(tin["q_idx"], tin["q_scale"], self.k_pool, self.k_scale, self.seqs, self.stride, self.k,
+                              o_idx, self.lens)
+            if ev is not None:
+                ev[1].record(self.stream)
+                ev[2].record(self.stream)
+        elif self.has_idx:
             smla.indexer_scores(tin["q_idx"], tin["q_scale"], self.k_pool, self.k_scale, self.seqs, self.scores)
             if ev is not None:
                 ev[1].record(self.stream)
@@ -339,8 +365,17 @@ class Case:
             if ev is not None:
                 ev[2].record(self.stream)
         if self.has_attn:
-            smla.sparse_prefill(tin["q_attn"], self.latent, self.scales, w.scale_block_size, o_idx, self.lens,
-                                w.softmax_scale, o_out)
+            if self.attn == "dense":
+                smla.dense_prefill(tin["q_attn"], self.latent, self.scales, w.scale_block_size, self.seqs,
+                                   w.softmax_scale, o_out)
+            elif self.attn == "decode":
+                smla.sparse_decode(tin["q_attn"], self.latent, self.scales, w.scale_block_size, o_idx, self.lens,
+                                   w.softmax_scale, o_out, self.ws)
+            elif self.attn == "bf16cache":
+                smla.sparse_prefill_bf16_cache(tin["q_attn"], self.latent, o_idx, self.lens, w.softmax_scale, o_out)
+            else:
+                smla.sparse_prefill(tin["q_attn"], self.latent, self.scales, w.scale_block_size, o_idx, self.lens,
+                                    w.softmax_scale, o_out)
             if ev is not None:
                 ev[3].record(self.stream)
 
@@ -383,7 +418,9 @@ class Case:
         total_ms = e0.elapsed_time(e1)
         stage = {}
         if g is None:
-            if self.has_idx:
+            if self.fused:
+                stage["indexer_topk"] = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+            elif self.has_idx:
                 stage["indexer"] = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
                 stage["topk"] = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
             if self.has_attn:
@@ -511,7 +548,8 @@ def run_ours(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    c = Case(args.case, dev)
+    # the step: fused indexer + top-k (score rows on chip), then attention
+    c = Case(args.case, dev, fused=not args.unfused)
     w = c.w
     sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", 0)))
     total_ms, stage, clocks = c.time_steps(args.steps, args.warmup, graph=args.graph, world=world, sampler=sampler)
@@ -523,34 +561,50 @@ def run_ours(args, rank, world):
             stage[x] = red[i + 1]
     ms_step = total_ms / args.steps
     e2e = None if args.no_e2e else c.e2e(args.steps, world)
-    c_flops = c.flops
+    c_flops, n_kernels = c.flops, c.n_kernels
+    # the standalone indexer and top-k on the same inputs (stage breakdown)
+    unfused = {}
+    if c.fused and not args.graph:
+        c.fused = False
+        _, ust, _ = c.time_steps(max(5, args.steps // 2), 2)
+        unfused = {k_: ust[k_] for k_ in ("indexer", "topk")}
+        c.fused = True
 
-    # the other attention workloads, kernel time only (same launch as the tests)
+    # the other workloads, in the same launch configuration as the tests
     extra = {}
     if not args.no_extra and args.case == "chunk":
         c.free()
         del c
-        for name in ("dsv32", "blockwise"):
-            x = Case(name, dev)
-            t, st, _ = x.time_steps(max(5, args.steps // 2), args.warmup)
-            extra[name] = (x.w, x.flops, st["sparse_mla"], t)
+        for name, graph in (("dsv32", False), ("blockwise", False), ("dsv32_bf16cache", False), ("dense", False),
+                            ("decode", True), ("mtp_decode", True), ("tiny", True)):
+            x = Case(name, dev, fused=True)
+            reps = max(5, args.steps // 2) if not graph else 200
+            t, st, _ = x.time_steps(reps, args.warmup, graph=graph)
+            extra[name] = (x, t / reps, st)
             x.free()
-            del x
     if rank != 0:
         return
     peaks, src = load_peaks()
     hbm = peak_value(peaks, "hbm_gbs")
+    fp8_peak_burst = 2.0 * peak_value(peaks, "bf16_tflops")
     fp8_q = w.q_dtype == 1
     stages = {}
-    if "indexer" in stage:
-        idx_bytes = w.q_idx.nbytes + w.q_scale.nbytes + w.k_pool.nbytes + w.k_scale.nbytes + 4 * c_kt(w)
-        fp8_peak = 2.0 * peak_value(peaks, "bf16_tflops")
-        tf_idx = 1e-12 * c_kt(w) * w.h_idx * 256 / (stage["indexer"] * 1e-3)
-        stages["indexer"] = {"ms": stage["indexer"], "TFLOP/s": tf_idx, "frac_fp8_peak": tf_idx / fp8_peak,
-                             "GB/s_algorithmic": 1e-9 * idx_bytes / (stage["indexer"] * 1e-3)}
-        topk_bytes = 4 * c_kt(w) + 4 * w.seqs.T * w.topk + 4 * w.seqs.T
-        gbs = 1e-9 * topk_bytes / (stage["topk"] * 1e-3)
-        stages["topk"] = {"ms": stage["topk"], "GB/s_algorithmic": gbs, "frac_hbm": gbs / hbm}
+    kt = c_kt(w)
+    if "indexer_topk" in stage:
+        tf_idx = 1e-12 * kt * w.h_idx * 256 / (stage["indexer_topk"] * 1e-3)
+        stages["indexer_topk"] = {"ms": stage["indexer_topk"], "keys_tok_per_s": kt / (stage["indexer_topk"] * 1e-3),
+                                  "indexer_TFLOP/s": tf_idx, "frac_fp8_peak": tf_idx / fp8_peak_burst,
+                                  "entry": "smla_indexer_topk (score rows on chip)"}
+    if unfused or "indexer" in stage:
+        u = unfused or {k_: stage[k_] for k_ in ("indexer", "topk")}
+        idx_bytes = w.q_idx.nbytes + w.q_scale.nbytes + w.k_pool.nbytes + w.k_scale.nbytes + 4 * kt
+        tf_idx = 1e-12 * kt * w.h_idx * 256 / (u["indexer"] * 1e-3)
+        topk_bytes = 4 * kt + 4 * w.seqs.T * w.topk + 4 * w.seqs.T
+        gbs = 1e-9 * topk_bytes / (u["topk"] * 1e-3)
+        stages["unfused"] = {
+            "indexer": {"ms": u["indexer"], "TFLOP/s": tf_idx, "frac_fp8_peak": tf_idx / fp8_peak_burst,
+                        "GB/s_algorithmic": 1e-9 * idx_bytes / (u["indexer"] * 1e-3)},
+            "topk": {"ms": u["topk"], "GB/s_algorithmic": gbs, "frac_hbm": gbs / hbm}}
     flops = c_flops
     if "sparse_mla" in stage:
         tf = flops / (stage["sparse_mla"] * 1e-3) / 1e12
@@ -562,7 +616,7 @@ def run_ours(args, rank, world):
     if w.H:
         value, unit = weak_scaling_value(world, flops, ms_step) / 1e12, "TFLOP/s"
     else:
-        value, unit = weak_scaling_value(world, c_kt(w), ms_step), "keys·tok/s"
+        value, unit = weak_scaling_value(world, kt, ms_step), "keys·tok/s"
     line = {
         "metric": METRIC,
         "value": value,
@@ -578,14 +632,16 @@ def run_ours(args, rank, world):
         "data": "synthetic",
         "config": config_dict(w, world),
         "stages": stages,
-        "gpu_launches": (2 if w.h_idx else 0) * args.steps + (1 if w.H else 0) * args.steps,
+        "gpu_launches": n_kernels * args.steps,
         "clocks": clocks,
     }
+    line["config"]["step"] = ("smla_indexer_topk -> smla_sparse_prefill" if not args.unfused else
+                              "smla_indexer_scores -> smla_topk -> smla_sparse_prefill")
     if args.graph:
         line["config"]["launch"] = "CUDA graph replay of one step"
-    if "indexer" in stage:
-        line["indexer_topk"] = {"value": world * c_kt(w) / ((stage["indexer"] + stage["topk"]) * 1e-3),
-                                "unit": "keys·tok/s"}
+    if w.h_idx:
+        ms_it = stage.get("indexer_topk", stage.get("indexer", 0.0) + stage.get("topk", 0.0)) or ms_step
+        line["indexer_topk"] = {"value": world * kt / (ms_it * 1e-3), "unit": "keys·tok/s"}
     if "sparse_mla" in stage:
         tf = stages["sparse_mla"]["TFLOP/s"]
         traffic = profiled_traffic("serving_fp8_indexer_gb300/csrc/prefill.cu", attn_variant(w), int(w.seqs.T))
@@ -598,19 +654,32 @@ def run_ours(args, rank, world):
                                        "achieved": tf * r, "peak": fp8_attn_peak,
                                        "frac": tf * r / fp8_attn_peak}}
     elif "topk" in stage:
-        line["roofline"] = {"bound": "hbm", "kernel": "topk_kernel", "achieved": stages["topk"]["GB/s_algorithmic"],
-                            "peak": hbm, "unit": "GB/s", "frac": stages["topk"]["frac_hbm"], "traffic": None,
+        line["roofline"] = {"bound": "hbm", "kernel": "topk_kernel", "achieved": stages["unfused"]["topk"]["GB/s_algorithmic"],
+                            "peak": hbm, "unit": "GB/s", "frac": stages["unfused"]["topk"]["frac_hbm"], "traffic": None,
                             "peak_source": f"{src} HBM copy"}
     if extra:
         line["other_workloads"] = {}
-        for name, (xw, xf, ms, t) in extra.items():
-            xfp8 = xw.q_dtype == 1
-            pk, pn = attn_peaks(peaks, src, xfp8, t * 1e-3)
-            tf = xf / (ms * 1e-3) / 1e12
-            line["other_workloads"][name] = {
-                "workload": xw.name, "stage": "sparse_mla", "ms": ms, "TFLOP/s": tf, "frac_peak": tf / pk,
-                "peak_source": pn, "issued_frac_fp8": tf * issued_ratio(xw) / (pk if xfp8 else 2.0 * pk),
-                "dtype": dtype_label(xw)}
+        for name, (x, ms_rep, st) in extra.items():
+            xw = x.w
+            d = {"workload": xw.name, "entry": {"sparse": "smla_sparse_prefill", "dense": "smla_dense_prefill",
+                                                "decode": "smla_sparse_decode (split-K)",
+                                                "bf16cache": "smla_sparse_prefill_bf16_cache"}[x.attn]
+                 if xw.H else "smla_indexer_topk", "dtype": dtype_label(xw)}
+            if x.has_attn:
+                ms = st.get("sparse_mla", ms_rep)
+                xfp8 = xw.q_dtype == 1
+                pk, pn = attn_peaks(peaks, src, xfp8, ms * 1e-3 * max(5, args.steps // 2))
+                tf = x.flops / (ms * 1e-3) / 1e12
+                d.update({"stage": "attention", "ms": ms, "TFLOP/s": tf, "frac_peak": tf / pk, "peak_source": pn})
+                if x.attn != "bf16cache":
+                    d["issued_frac_fp8"] = tf * issued_ratio(xw) / (pk if xfp8 else 2.0 * pk)
+            if x.has_idx and not x.has_attn:
+                d.update({"stage": "indexer + top-k", "ms": ms_rep, "keys_tok_per_s": x.kt / (ms_rep * 1e-3)})
+            if x.has_idx and x.has_attn:
+                d["whole_path_ms"] = ms_rep
+            if name in ("decode", "mtp_decode", "tiny"):
+                d["launch"] = "CUDA graph replay, 200 steps (launch-latency regime)"
+            line["other_workloads"][name] = d
     if e2e is not None:
         line["e2e"] = e2e
     if world == 1 and not args.no_cpu_baseline and args.case == "chunk":
@@ -637,7 +706,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", choices=sorted(CASES), default="chunk")
     ap.add_argument("--graph", action="store_true", help="replay each step as a CUDA graph")
-    ap.add_argument("--no-extra", action="store_true", help="skip the other attention workloads")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--unfused", action="store_true", help="indexer and top-k as two kernels (score buffer in HBM)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -238,11 +238,11 @@ def mtp_decode_indexer(seed=1) -> Workload:
     return build("mtp_decode_B8x2_L2048_Hidx64", seed, [2] * 8, [2048] * 8, 64, h_idx=64, topk=2048)
 
 
-def dsv32_prefill(seed=2, T=4096, k=2048) -> Workload:
+def dsv32_prefill(seed=2, T=4096, k=2048, latent_bf16=False) -> Workload:
     """1 sequence of T tokens (positions 0..T-1), H=128 bf16 Q, unit-scale
-    e4m3 latent, top-k causally sampled indices."""
-    return build(f"sparse_prefill_T{T}_H128_bf16_unit_k{k}", seed, [T], [T], 64, topk=k, H=128,
-                 q_dtype=Q_BF16, sbs=0, sample_indices=True)
+    e4m3 latent (or a BF16 latent cache), top-k causally sampled indices."""
+    return build(f"sparse_prefill_T{T}_H128_bf16_{'bf16cache' if latent_bf16 else 'unit'}_k{k}", seed, [T], [T], 64,
+                 topk=k, H=128, q_dtype=Q_BF16, sbs=0, sample_indices=True, latent_bf16=latent_bf16)
 
 
 def blockwise_fp8_prefill(seed=3, lens=(1024, 2048, 3072, 4096), k=2048) -> Workload:
