@@ -170,6 +170,9 @@ CASES = {
     # the same shapes with one sequence of 1024 new tokens (inputs still
     # larger than L2), for ncu captures
     "chunk_small": ("e2e_chunk", dict(B=1, q_len=1024)),
+    # two sequences of 2048 new tokens (4096 tokens: q 604 MB and the output
+    # 537 MB exceed L2), for DRAM-traffic captures
+    "chunk_4k": ("e2e_chunk", dict(B=2)),
     # the other workloads, stage by stage
     "tiny": ("tiny_prefill", dict()),
     "mtp_decode": ("mtp_decode_indexer", dict()),
@@ -548,8 +551,9 @@ def run_ours(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    # the step: fused indexer + top-k (score rows on chip), then attention
-    c = Case(args.case, dev, fused=not args.unfused)
+    # the step: indexer -> top-k -> attention (--fused: indexer + top-k as one
+    # kernel with the score rows on chip)
+    c = Case(args.case, dev, fused=args.fused)
     w = c.w
     sampler = ClockSampler(int(os.environ.get("LOCAL_RANK", 0)))
     total_ms, stage, clocks = c.time_steps(args.steps, args.warmup, graph=args.graph, world=world, sampler=sampler)
@@ -562,13 +566,13 @@ def run_ours(args, rank, world):
     ms_step = total_ms / args.steps
     e2e = None if args.no_e2e else c.e2e(args.steps, world)
     c_flops, n_kernels = c.flops, c.n_kernels
-    # the standalone indexer and top-k on the same inputs (stage breakdown)
-    unfused = {}
-    if c.fused and not args.graph:
-        c.fused = False
-        _, ust, _ = c.time_steps(max(5, args.steps // 2), 2)
-        unfused = {k_: ust[k_] for k_ in ("indexer", "topk")}
-        c.fused = True
+    # the other form of indexer + top-k on the same inputs
+    other_form = {}
+    if c.has_idx and not args.graph:
+        c.fused = not c.fused
+        _, ost, _ = c.time_steps(max(5, args.steps // 2), 2)
+        other_form = ost
+        c.fused = not c.fused
 
     # the other workloads, in the same launch configuration as the tests
     extra = {}
@@ -590,21 +594,22 @@ def run_ours(args, rank, world):
     fp8_q = w.q_dtype == 1
     stages = {}
     kt = c_kt(w)
-    if "indexer_topk" in stage:
-        tf_idx = 1e-12 * kt * w.h_idx * 256 / (stage["indexer_topk"] * 1e-3)
-        stages["indexer_topk"] = {"ms": stage["indexer_topk"], "keys_tok_per_s": kt / (stage["indexer_topk"] * 1e-3),
-                                  "indexer_TFLOP/s": tf_idx, "frac_fp8_peak": tf_idx / fp8_peak_burst,
-                                  "entry": "smla_indexer_topk (score rows on chip)"}
-    if unfused or "indexer" in stage:
-        u = unfused or {k_: stage[k_] for k_ in ("indexer", "topk")}
+    fused_ms = stage.get("indexer_topk", other_form.get("indexer_topk"))
+    if fused_ms:
+        tf_idx = 1e-12 * kt * w.h_idx * 256 / (fused_ms * 1e-3)
+        stages["fused_indexer_topk"] = {"ms": fused_ms, "keys_tok_per_s": kt / (fused_ms * 1e-3),
+                                        "indexer_TFLOP/s": tf_idx, "frac_fp8_peak": tf_idx / fp8_peak_burst,
+                                        "entry": "smla_indexer_topk (score rows on chip)",
+                                        "in_step": "indexer_topk" in stage}
+    if "indexer" in stage or "indexer" in other_form:
+        u = stage if "indexer" in stage else other_form
         idx_bytes = w.q_idx.nbytes + w.q_scale.nbytes + w.k_pool.nbytes + w.k_scale.nbytes + 4 * kt
         tf_idx = 1e-12 * kt * w.h_idx * 256 / (u["indexer"] * 1e-3)
         topk_bytes = 4 * kt + 4 * w.seqs.T * w.topk + 4 * w.seqs.T
         gbs = 1e-9 * topk_bytes / (u["topk"] * 1e-3)
-        stages["unfused"] = {
-            "indexer": {"ms": u["indexer"], "TFLOP/s": tf_idx, "frac_fp8_peak": tf_idx / fp8_peak_burst,
-                        "GB/s_algorithmic": 1e-9 * idx_bytes / (u["indexer"] * 1e-3)},
-            "topk": {"ms": u["topk"], "GB/s_algorithmic": gbs, "frac_hbm": gbs / hbm}}
+        stages["indexer"] = {"ms": u["indexer"], "TFLOP/s": tf_idx, "frac_fp8_peak": tf_idx / fp8_peak_burst,
+                             "GB/s_algorithmic": 1e-9 * idx_bytes / (u["indexer"] * 1e-3), "in_step": "indexer" in stage}
+        stages["topk"] = {"ms": u["topk"], "GB/s_algorithmic": gbs, "frac_hbm": gbs / hbm, "in_step": "topk" in stage}
     flops = c_flops
     if "sparse_mla" in stage:
         tf = flops / (stage["sparse_mla"] * 1e-3) / 1e12
@@ -635,7 +640,7 @@ def run_ours(args, rank, world):
         "gpu_launches": n_kernels * args.steps,
         "clocks": clocks,
     }
-    line["config"]["step"] = ("smla_indexer_topk -> smla_sparse_prefill" if not args.unfused else
+    line["config"]["step"] = ("smla_indexer_topk -> smla_sparse_prefill" if args.fused else
                               "smla_indexer_scores -> smla_topk -> smla_sparse_prefill")
     if args.graph:
         line["config"]["launch"] = "CUDA graph replay of one step"
@@ -654,8 +659,8 @@ def run_ours(args, rank, world):
                                        "achieved": tf * r, "peak": fp8_attn_peak,
                                        "frac": tf * r / fp8_attn_peak}}
     elif "topk" in stage:
-        line["roofline"] = {"bound": "hbm", "kernel": "topk_kernel", "achieved": stages["unfused"]["topk"]["GB/s_algorithmic"],
-                            "peak": hbm, "unit": "GB/s", "frac": stages["unfused"]["topk"]["frac_hbm"], "traffic": None,
+        line["roofline"] = {"bound": "hbm", "kernel": "topk_kernel", "achieved": stages["topk"]["GB/s_algorithmic"],
+                            "peak": hbm, "unit": "GB/s", "frac": stages["topk"]["frac_hbm"], "traffic": None,
                             "peak_source": f"{src} HBM copy"}
     if extra:
         line["other_workloads"] = {}
@@ -707,7 +712,7 @@ def main():
     ap.add_argument("--case", choices=sorted(CASES), default="chunk")
     ap.add_argument("--graph", action="store_true", help="replay each step as a CUDA graph")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
-    ap.add_argument("--unfused", action="store_true", help="indexer and top-k as two kernels (score buffer in HBM)")
+    ap.add_argument("--fused", action="store_true", help="indexer + top-k as one kernel (score rows on chip)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
