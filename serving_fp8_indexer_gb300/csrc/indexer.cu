@@ -385,7 +385,8 @@ smla_status_t launch_indexer(const uint8_t* q, const float* q_scale, const uint8
   // Key chunk per work item: enough items to give every SM about two.
   const int64_t key_tiles = (score_stride + kBM - 1) / kBM;
   const int64_t est_tt = (seqs.T + tok - 1) / tok;
-  int64_t chunk = (est_tt * key_tiles + 2 * 152 - 1) / (2 * 152);
+  const int64_t want = 2 * static_cast<int64_t>(device_sm_count());
+  int64_t chunk = (est_tt * key_tiles + want - 1) / want;
   chunk = std::max<int64_t>(1, std::min<int64_t>(chunk, key_tiles));
   // the item's page ids are staged in shared memory (kMaxItemPages)
   chunk = std::min<int64_t>(chunk, static_cast<int64_t>(kMaxItemPages - 2) * seqs.page_size / kBM);

@@ -309,6 +309,35 @@ __device__ __forceinline__ void issue_qk(uint32_t s_tmem, uint64_t a0, uint64_t 
       }
 }
 
+// Split-K: the item's normalised partial output O^T / l as f32, thread = one
+// value column of 32 heads (a warp store covers 32 consecutive columns of one
+// head); heads from nh on are outside the item.  Out of line: the split path
+// is rare, and inlined it cost the block loop registers (measured 2 % on the
+// end-to-end chunk).
+__device__ __noinline__ void store_partial(float* po, uint32_t taddr, const float* linv, int nh) {
+#pragma unroll 1
+  for (int tile = 0; tile < 4; ++tile) {
+    uint32_t v[32];
+    tmem_ld32(taddr + tile * kNH, v);
+    tmem_wait_ld();
+#pragma unroll
+    for (int h = 0; h < 32; ++h)
+      if (h < nh) __stcs(po + static_cast<int64_t>(h) * kDV + tile * 128, __uint_as_float(v[h]) * linv[h]);
+  }
+}
+
+// The row sum l = sum_j exp2(z_j - m) of one head (negm = -m, log2 units)
+// in the two rarer modes: split-K writes the partial's log2-sum-exp m +
+// log2 l to part_lse[prow] (the combine adds the sink); otherwise the sink
+// term exp2(sink * log2e - m) joins l.  Out of line, like store_partial.
+__device__ __noinline__ float split_or_sink(const Params& p, int64_t prow, int head, float l, float negm) {
+  if (p.nsplit > 1) {
+    p.part_lse[prow] = l > 0.f ? log2f(l) - negm : -INFINITY;
+    return l;
+  }
+  return l + ex2_approx(fmaf(p.sink[head], kLog2e, negm));
+}
+
 // One work item: a token, one group of 64 heads and (split-K) one range of
 // the token's key blocks.
 struct Item {
@@ -543,6 +572,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
       const int wn = w + static_cast<int>(gridDim.x);  // this CTA's next item
       const int n = I.n, nblk = I.nblk;
+      const int n_item = n - I.j0 * kBK;  // the token's keys from this item's first block on
       uint16_t* out_t = p.out + (static_cast<int64_t>(I.t) * p.H + I.h0) * kDV;
       // split-K partials of this item: rows (t * nsplit + s) * H + h of
       // [T, nsplit, H, 512] and [T, nsplit, H]
@@ -637,8 +667,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
             }
           }
         }
-        const int jg = I.j0 + j;  // block index among the token's blocks
-        if ((jg + 1) * kBK > n && jg * kBK + r >= n) {  // lanes past the token's keys (its last block only)
+        if ((j + 1) * kBK > n_item && j * kBK + r >= n_item) {  // lanes past the token's keys (its last block only)
 #pragma unroll
           for (int h = 0; h < 32; ++h) y[h] = -INFINITY;
           ymax = -INFINITY;
@@ -785,29 +814,14 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
       if (threadIdx.x < kNH) {
         // l = sum_j exp2(z_j - m); the reference m is -negm (log2 units)
         float l = linv[threadIdx.x];
-        if (p.nsplit > 1) {
-          // split partial: log2-sum-exp m + log2 l (the combine adds the sink)
-          if (threadIdx.x < I.hv) p.part_lse[part_row() + threadIdx.x] = l > 0.f ? log2f(l) - s.negm[threadIdx.x] : -INFINITY;
-        } else if (p.sink != nullptr && threadIdx.x < I.hv) {
-          l += ex2_approx(fmaf(p.sink[I.h0 + threadIdx.x], kLog2e, s.negm[threadIdx.x]));
-        }
+        if ((p.nsplit > 1 || p.sink != nullptr) && threadIdx.x < I.hv)
+          l = split_or_sink(p, part_row() + threadIdx.x, I.h0 + threadIdx.x, l, s.negm[threadIdx.x]);
         linv[threadIdx.x] = l > 0.f ? 1.f / l : 0.f;
       }
       named_bar_sync(1, kSoftThreads);
       if (done && p.nsplit > 1) {
         tc_fence_after();
-        // normalised partial O, f32: thread = one value column, a warp store
-        // covers 32 consecutive columns of one head
-        float* po = p.part_o + part_row() * kDV + r;
-#pragma unroll 1
-        for (int tile = 0; tile < 4; ++tile) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + tile * kNH + hb, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int h = 0; h < 32; ++h)
-            if (hb + h < I.hv) __stcs(po + static_cast<int64_t>(hb + h) * kDV + tile * 128, __uint_as_float(v[h]) * linv[hb + h]);
-        }
+        store_partial(p.part_o + (part_row() + hb) * kDV + r, tmem + lane_base + hb, linv + hb, I.hv - hb);
       } else if (done) {
         tc_fence_after();
         // thread = one value column.  Lane pairs swap one value per two heads,
