@@ -19,7 +19,7 @@
 // key order; it emits physical rows (page table) and topk_lengths, and ties
 // at the k-th value go to the lower logical key, as smla_topk does.
 //
-// Warp roles (16 warps, 128 registers a thread): 0 TMA producer (q per
+// Warp roles (20 warps): 0 TMA producer (q per
 // tile, K tiles through the page table), 1 MMA issuer and TMEM owner, 2-3
 // idle, 4-11 epilogue (TMEM lane quarter x 64-column half), 12-15
 // selectors.
@@ -36,22 +36,29 @@ constexpr int kBM = 128;                  // keys per tile (MMA M)
 constexpr int kBN = 128;                  // (token, head) columns per tile (MMA N)
 constexpr int kStages = 3;                // K tile ring
 constexpr int kEpiWarps = 8;
-constexpr int kSelWarps = 4;
+constexpr int kSelGroups = 2;             // selector groups: one token of a tile each at a time
+constexpr int kGrpWarps = 4;
+constexpr int kGrpThreads = 32 * kGrpWarps;
+constexpr int kSelWarps = kSelGroups * kGrpWarps;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kSelThreads = 32 * kSelWarps;
 constexpr int kEpiWarp0 = 4;
 constexpr int kSelWarp0 = kEpiWarp0 + kEpiWarps;
 constexpr int kThreads = 32 * (kSelWarp0 + kSelWarps);
-static_assert(kThreads == 512 && kEpiWarp0 % 4 == 0, "epilogue warp w reads TMEM lane quarter w % 4");
+static_assert(kThreads == 640 && kEpiWarp0 % 4 == 0, "epilogue warp w reads TMEM lane quarter w % 4");
 constexpr int kSliceCols = kBN / 2;       // columns per epilogue warp
 constexpr int kRowCap = 16384;            // floats per score buffer (TOK rows of L)
 constexpr int kMaxPages = 1024;           // page ids staged per tile
 constexpr int kBins = 2048;               // 11-bit digits
-constexpr int kBinsPerThread = kBins / kSelThreads;
+constexpr int kBinsPerThread = kBins / kGrpThreads;
 constexpr int kMaxE4 = 16;                // float4 groups per selector thread (rows of <= 8192 keys)
-constexpr uint32_t kTmemCols = 2 * kBN;
-constexpr int kBarEpi = 1, kBarSel = 2;   // named barriers
-static_assert(kSelThreads * 4 * kMaxE4 == 8192, "the selectors' per-group counts cover a row of 8192 keys");
+// TMEM accumulators (measured on the end-to-end chunk: four, letting the
+// MMA run three tiles ahead, 2.464 ms; two 2.467 ms)
+constexpr int kAcc = 2;
+constexpr uint32_t kTmemCols = kAcc * kBN;
+constexpr int kBarEpi = 1, kBarSel0 = 2;  // named barriers: epilogue, selector group g at kBarSel0 + g
+constexpr int kMaxTok = kBN / 4;          // tokens per tile at the smallest H_idx
+static_assert(kGrpThreads * 4 * kMaxE4 == 8192, "a selector group's per-group counts cover a row of 8192 keys");
 
 struct Params {
   const float* q_scale;
@@ -75,13 +82,17 @@ struct __align__(1024) Smem {
   float scores[2][kRowCap];          // [buffer][token * L + key]
   int pages[2][kMaxPages];           // the tile's sequence page ids, per score buffer
   int ppages[kMaxPages];             // the producer's copy for the tile it is loading
-  uint32_t hist[kBins];
+  struct Sel {  // one selector group's scratch
+    uint32_t hist[kBins];
+    uint32_t cnt_w[kMaxE4][kGrpWarps];  // per (float4 group, warp): gt count | tie count << 16
+    int wtot[kGrpWarps + 1];
+    int sh_bin, sh_above, sh_cnt;
+  } sel[kSelGroups];
   float qs[kBN];
-  uint32_t cnt_w[kMaxE4][kSelWarps];  // per (float4 group, warp): gt count | tie count << 16
-  int wtot[kSelWarps + 1];
-  uint32_t wmin[kSelWarps], wmax[kSelWarps];
-  int sh_bin, sh_above, sh_cnt;
-  unsigned long long bar_q, bar_qfree, bar_kfull[kStages], bar_kempty[kStages], bar_afull[2], bar_aempty[2];
+  // each token's smallest and largest score of the tile (order-preserving
+  // keys), taken by the epilogue while it writes the rows
+  uint32_t tmin[2][kMaxTok], tmax[2][kMaxTok];
+  unsigned long long bar_q, bar_qfree, bar_kfull[kStages], bar_kempty[kStages], bar_afull[kAcc], bar_aempty[kAcc];
   unsigned long long bar_sfull[2], bar_sfree[2], bar_drain;
   uint32_t tmem_base;
   int k_issued, k_landed, q_issued, q_landed;
@@ -150,79 +161,56 @@ __device__ __forceinline__ uint32_t phys_of(const int* pages, int shift, int key
   return pid < 0 ? 0xFFFFFFFFu : (static_cast<uint32_t>(pid) << shift) | static_cast<uint32_t>(key & ((1 << shift) - 1));
 }
 
-// Exclusive prefix over the selector threads of v (thread order); returns it
-// and leaves the total in s.wtot[kSelWarps].
-__device__ __forceinline__ int sel_scan(Smem& s, int v) {
-  const int tid = threadIdx.x - kSelWarp0 * 32, lane = tid & 31, wp = tid >> 5;
+// Exclusive prefix of v over a selector group's threads (thread order);
+// returns it and leaves the total in g.wtot[kGrpWarps].  tid: the thread's
+// index in the group; bar: the group's named barrier.
+__device__ __forceinline__ int sel_scan(Smem::Sel& g, int v, int tid, int bar) {
+  const int lane = tid & 31, wp = tid >> 5;
   int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const int x = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += x;
   }
-  if (lane == 31) s.wtot[wp] = incl;
-  named_bar_sync(kBarSel, kSelThreads);
+  if (lane == 31) g.wtot[wp] = incl;
+  named_bar_sync(bar, kGrpThreads);
   if (tid == 0) {
     int run = 0;
-    for (int i = 0; i < kSelWarps; ++i) {
-      const int x = s.wtot[i];
-      s.wtot[i] = run;
+    for (int i = 0; i < kGrpWarps; ++i) {
+      const int x = g.wtot[i];
+      g.wtot[i] = run;
       run += x;
     }
-    s.wtot[kSelWarps] = run;
+    g.wtot[kGrpWarps] = run;
   }
-  named_bar_sync(kBarSel, kSelThreads);
-  return s.wtot[wp] + incl - v;
+  named_bar_sync(bar, kGrpThreads);
+  return g.wtot[wp] + incl - v;
 }
 
-// Top-k of one score row in shared memory (n > k valid keys) by the selector
-// warps: writes the physical rows of the k selected keys, in ascending
-// logical-key order, to out[0..k).  Thread tid handles the keys
-// 4 * (e * 128 + tid) + u (u < 4) of every float4 group e; each pass reads
-// them again from the row (conflict-free float4 loads) rather than holding
-// them in registers.
-__device__ __forceinline__ void select_row(Smem& s, const float* row, int n, int k, const int* pages, int shift,
-                                           uint32_t* out, unsigned* err) {
-  const int tid = threadIdx.x - kSelWarp0 * 32, lane = tid & 31, wp = tid >> 5;
-  const int E4 = (n + 4 * kSelThreads - 1) / (4 * kSelThreads);
+// Top-k of one score row in shared memory (n > k valid keys) by one selector
+// group: writes the physical rows of the k selected keys, in ascending
+// logical-key order, to out[0..k).  kmin / kmax: the row's smallest and
+// largest order-preserving keys (taken by the epilogue).  Thread tid (of the
+// group's 128) handles the keys 4 * (e * 128 + tid) + u (u < 4) of every
+// float4 group e; each pass reads them again from the row (conflict-free
+// float4 loads) rather than holding them in registers.
+__device__ __forceinline__ void select_row(Smem::Sel& g, int tid, int bar, const float* row, int n, int k,
+                                           uint32_t kmin, uint32_t kmax, const int* pages, int shift, uint32_t* out,
+                                           unsigned* err) {
+  const int lane = tid & 31, wp = tid >> 5;
+  const int E4 = (n + 4 * kGrpThreads - 1) / (4 * kGrpThreads);
   const float4* row4 = reinterpret_cast<const float4*>(row);
   // this thread's four keys of group e, as ordered keys, and how many of the
   // four are valid
   auto group = [&](int e, uint32_t (&u)[4]) -> int {
-    const int key0 = 4 * (e * kSelThreads + tid);
-    const float4 v = row4[e * kSelThreads + tid];  // inside the row: key0 + 3 < L
+    const int key0 = 4 * (e * kGrpThreads + tid);
+    const float4 v = row4[e * kGrpThreads + tid];  // inside the row: key0 + 3 < L
     u[0] = ordered(v.x);
     u[1] = ordered(v.y);
     u[2] = ordered(v.z);
     u[3] = ordered(v.w);
     return min(4, max(0, n - key0));
   };
-  uint32_t kmin = 0xffffffffu, kmax = 0u;
-#pragma unroll 1
-  for (int e = 0; e < E4; ++e) {
-    uint32_t u[4];
-    const int nv = group(e, u);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (q < nv) {
-        kmin = min(kmin, u[q]);
-        kmax = max(kmax, u[q]);
-      }
-  }
-  kmin = __reduce_min_sync(0xffffffffu, kmin);
-  kmax = __reduce_max_sync(0xffffffffu, kmax);
-  if (lane == 0) {
-    s.wmin[wp] = kmin;
-    s.wmax[wp] = kmax;
-  }
-  named_bar_sync(kBarSel, kSelThreads);
-  kmin = s.wmin[0];
-  kmax = s.wmax[0];
-#pragma unroll
-  for (int w = 1; w < kSelWarps; ++w) {
-    kmin = min(kmin, s.wmin[w]);
-    kmax = max(kmax, s.wmax[w]);
-  }
   // ---- digits: keys matching (hi_mask, hi_val) are the candidates, krem of
   // them still to be taken
   int krem = k;
@@ -236,39 +224,39 @@ __device__ __forceinline__ void select_row(Smem& s, const float* row, int n, int
     while (top >= 0) {
       const int sh = max(0, top - 10);
       const uint32_t dmask = (1u << (top - sh + 1)) - 1u;
-      named_bar_sync(kBarSel, kSelThreads);  // readers of the previous histogram are done
-      for (int i = tid; i < kBins; i += kSelThreads) s.hist[i] = 0;
-      named_bar_sync(kBarSel, kSelThreads);
-#pragma unroll 1
+      named_bar_sync(bar, kGrpThreads);  // readers of the previous histogram are done
+      for (int i = tid; i < kBins; i += kGrpThreads) g.hist[i] = 0;
+      named_bar_sync(bar, kGrpThreads);
+#pragma unroll 4
       for (int e = 0; e < E4; ++e) {
         uint32_t u[4];
         const int nv = group(e, u);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          if (q < nv && (u[q] & hi_mask) == hi_val) atomicAdd(&s.hist[(u[q] >> sh) & dmask], 1u);
+          if (q < nv && (u[q] & hi_mask) == hi_val) atomicAdd(&g.hist[(u[q] >> sh) & dmask], 1u);
       }
-      named_bar_sync(kBarSel, kSelThreads);
+      named_bar_sync(bar, kGrpThreads);
       // bin of the krem-th largest candidate: thread rt owns bins [rt*16, rt*16+16)
-      const int rt = kSelThreads - 1 - tid;
+      const int rt = kGrpThreads - 1 - tid;
       int local = 0;
 #pragma unroll
-      for (int j = 0; j < kBinsPerThread; ++j) local += s.hist[rt * kBinsPerThread + j];
-      int c = sel_scan(s, local);
+      for (int j = 0; j < kBinsPerThread; ++j) local += g.hist[rt * kBinsPerThread + j];
+      int c = sel_scan(g, local, tid, bar);
 #pragma unroll
       for (int j = kBinsPerThread - 1; j >= 0; --j) {
         const int bin = rt * kBinsPerThread + j;
-        const int h = s.hist[bin];
+        const int h = g.hist[bin];
         if (c < krem && c + h >= krem) {
-          s.sh_bin = bin;
-          s.sh_above = c;
-          s.sh_cnt = h;
+          g.sh_bin = bin;
+          g.sh_above = c;
+          g.sh_cnt = h;
         }
         c += h;
       }
-      named_bar_sync(kBarSel, kSelThreads);
-      const int bin = s.sh_bin;
-      krem -= s.sh_above;
-      const int cnt = s.sh_cnt;
+      named_bar_sync(bar, kGrpThreads);
+      const int bin = g.sh_bin;
+      krem -= g.sh_above;
+      const int cnt = g.sh_cnt;
       hi_val |= static_cast<uint32_t>(bin) << sh;
       hi_mask |= dmask << sh;
       top = sh - 1;
@@ -312,19 +300,19 @@ __device__ __forceinline__ void select_row(Smem& s, const float* row, int n, int
     *tot = __shfl_sync(0xffffffffu, x, 31);
     return x - c;
   };
-#pragma unroll 1
+#pragma unroll 4
   for (int e = 0; e < kMaxE4; ++e) {
     uint32_t tot = 0u;
     if (e < E4) lane_prefix(flags(e), &tot);
-    if (lane == 0) s.cnt_w[e][wp] = (tot & 0xffu) | ((tot >> 8) << 16);
+    if (lane == 0) g.cnt_w[e][wp] = (tot & 0xffu) | ((tot >> 8) << 16);
   }
-  named_bar_sync(kBarSel, kSelThreads);
+  named_bar_sync(bar, kGrpThreads);
   if (tid < 32) {
     // exclusive prefix over (e, warp) in key order; both counts in one word
     uint32_t run = 0u;
-    for (int base = 0; base < kMaxE4 * kSelWarps; base += 32) {
+    for (int base = 0; base < kMaxE4 * kGrpWarps; base += 32) {
       const int idx = base + lane;
-      const uint32_t v = s.cnt_w[idx / kSelWarps][idx % kSelWarps];
+      const uint32_t v = g.cnt_w[idx / kGrpWarps][idx % kGrpWarps];
       uint32_t x = v;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -332,21 +320,21 @@ __device__ __forceinline__ void select_row(Smem& s, const float* row, int n, int
         if (lane >= o) x += y;
       }
       __syncwarp();
-      s.cnt_w[idx / kSelWarps][idx % kSelWarps] = run + x - v;
+      g.cnt_w[idx / kGrpWarps][idx % kGrpWarps] = run + x - v;
       run += __shfl_sync(0xffffffffu, x, 31);
     }
   }
-  named_bar_sync(kBarSel, kSelThreads);
-#pragma unroll 1
+  named_bar_sync(bar, kGrpThreads);
+#pragma unroll 2
   for (int e = 0; e < E4; ++e) {
     const uint32_t f = flags(e);
     uint32_t tot;
     const uint32_t lx = lane_prefix(f, &tot);
     if (f == 0u) continue;
-    const uint32_t cw = s.cnt_w[e][wp];
+    const uint32_t cw = g.cnt_w[e][wp];
     int gb = static_cast<int>((cw & 0xffffu) + (lx & 0xffu));
     int qb = static_cast<int>((cw >> 16) + ((lx >> 8) & 0xffu));
-    const int key0 = 4 * (e * kSelThreads + tid);
+    const int key0 = 4 * (e * kGrpThreads + tid);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const bool gt = (f >> j) & 1u, tie = (f >> (4 + j)) & 1u;
@@ -364,7 +352,7 @@ __device__ __forceinline__ void select_row(Smem& s, const float* row, int n, int
       qb += tie ? 1 : 0;
     }
   }
-  named_bar_sync(kBarSel, kSelThreads);  // s.cnt_w / hist are reused by the next row
+  named_bar_sync(bar, kGrpThreads);  // g.cnt_w / hist are reused by the next row
 }
 
 template <int HIDX>
@@ -385,9 +373,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&s.bar_kfull[i]), 1);
       mbar_init(smem_u32(&s.bar_kempty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kAcc; ++i) {
       mbar_init(smem_u32(&s.bar_afull[i]), 1);
       mbar_init(smem_u32(&s.bar_aempty[i]), kEpiThreads);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&s.bar_sfull[i]), kEpiThreads);
       mbar_init(smem_u32(&s.bar_sfree[i]), kSelThreads);
     }
@@ -477,13 +467,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) s.q_landed = it + 1;
         const uint32_t q_base = smem_u32(s.q);
         for (int i = 0; ok && i < x.nt; ++i, ++g) {
-          const int st = g % kStages, a = g & 1;
+          const int st = g % kStages, a = g % kAcc;
           if (!mbar_wait(smem_u32(&s.bar_kfull[st]), (g / kStages) & 1, p.err)) {
             ok = false;
             break;
           }
           s.k_landed = g + 1;
-          if (!mbar_wait(smem_u32(&s.bar_aempty[a]), ((g >> 1) & 1) ^ 1, p.err)) {
+          if (!mbar_wait(smem_u32(&s.bar_aempty[a]), ((g / kAcc) & 1) ^ 1, p.err)) {
             ok = false;
             break;
           }
@@ -536,6 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tok = et / HIDX, h = et % HIDX;
         s.qs[et] = tok < x.ntok ? p.q_scale[static_cast<int64_t>(x.t0 + tok) * HIDX + h] : 0.f;
       }
+      if (et < TOK) {
+        s.tmin[buf][et] = 0xffffffffu;
+        s.tmax[buf][et] = 0u;
+      }
       named_bar_sync(kBarEpi, kEpiThreads);
       const int* pg = s.pages[buf];
       const float* qs = s.qs + half * kSliceCols;
@@ -551,13 +545,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       float ks_next = load_ks(0), ks_next2 = load_ks(1);
       for (int i = 0; i < x.nt; ++i, ++g) {
-        const int a = g & 1;
+        const int a = g % kAcc;
         const float ks = ks_next;
         ks_next = ks_next2;
         ks_next2 = load_ks(i + 2);
         // warp-uniform (the tcgen05.ld below is warp-collective); a warp that
         // gives up leaves the loop, and the vote after it stops all of them
-        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_afull[a]), (g >> 1) & 1, p.err))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_afull[a]), (g / kAcc) & 1, p.err))) {
           ok = false;
           break;
         }
@@ -565,30 +559,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         float acc[SLICE_TOK];
 #pragma unroll
         for (int j = 0; j < SLICE_TOK; ++j) acc[j] = 0.f;
-        uint32_t v[64];
         const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * kBN + half * kSliceCols;
-        tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(v));
-        tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&s.bar_aempty[a]));  // the accumulator is in registers
         // relu, x q_scale, summed over each token's heads in head order (the
-        // standalone indexer's order, so both produce the same floats)
+        // standalone indexer's order, so both produce the same floats); 32
+        // columns a load
 #pragma unroll
-        for (int j = 0; j < kSliceCols; j += 4) {
-          const float4 q4 = *reinterpret_cast<const float4*>(qs + j);
-          const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+        for (int cb = 0; cb < kSliceCols; cb += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + cb, v);
+          tmem_wait_ld_regs(v);
+          if (cb + 32 == kSliceCols) {
+            tc_fence_before();
+            mbar_arrive(smem_u32(&s.bar_aempty[a]));  // the accumulator is in registers
+          }
 #pragma unroll
-          for (int uu = 0; uu < 4; ++uu) {
-            const int tj = (j + uu) / HIDX;
-            acc[tj] = fmaf(fmaxf(__uint_as_float(v[j + uu]), 0.f), qq[uu], acc[tj]);
+          for (int j = 0; j < 32; j += 4) {
+            const float4 q4 = *reinterpret_cast<const float4*>(qs + cb + j);
+            const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+            for (int uu = 0; uu < 4; ++uu) {
+              const int tj = (cb + j + uu) / HIDX;
+              acc[tj] = fmaf(fmaxf(__uint_as_float(v[j + uu]), 0.f), qq[uu], acc[tj]);
+            }
           }
         }
         const int key = i * kBM + row;
 #pragma unroll
         for (int j = 0; j < SLICE_TOK; ++j) {
           const int tok = half * SLICE_TOK + j;
-          if (tok < x.ntok && key <= x.pos0 + tok) srow[tok * L + key] = ks * acc[j];
+          const bool valid = tok < x.ntok && key <= x.pos0 + tok;
+          const float sc = ks * acc[j];
+          if (valid) srow[tok * L + key] = sc;
+          // the token's smallest and largest score so far (order-preserving keys)
+          const uint32_t u = ordered(sc);
+          const uint32_t wmn = __reduce_min_sync(0xffffffffu, valid ? u : 0xffffffffu);
+          const uint32_t wmx = __reduce_max_sync(0xffffffffu, valid ? u : 0u);
+          if (lane == 0 && tok < x.ntok && wmn <= wmx) {
+            atomicMin(&s.tmin[buf][tok], wmn);
+            atomicMax(&s.tmax[buf][tok], wmx);
+          }
         }
       }
       // every epilogue thread arrives here once per tile: a give-up by any
@@ -599,7 +608,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- selectors
-    const int st_id = threadIdx.x - kSelWarp0 * 32;
+    // group gi takes tokens gi, gi + 2, ... of each tile
+    const int gi = (warp - kSelWarp0) / kGrpWarps;
+    const int st_id = threadIdx.x - (kSelWarp0 + gi * kGrpWarps) * 32;
+    const int bar = kBarSel0 + gi;
+    Smem::Sel& sg = s.sel[gi];
     int it = 0;
     bool ok = true;
     for (int w = blockIdx.x; ok; w += gridDim.x, ++it) {
@@ -608,29 +621,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (b < 0) break;
       const Tile x = tile_make(p, b, tt, TOK);
       const int buf = it & 1;
-      if (!named_bar_and(kBarSel, kSelThreads, mbar_wait(smem_u32(&s.bar_sfull[buf]), (it >> 1) & 1, p.err))) {
+      if (!named_bar_and(bar, kGrpThreads, mbar_wait(smem_u32(&s.bar_sfull[buf]), (it >> 1) & 1, p.err))) {
         ok = false;
         break;
       }
       const int* pg = s.pages[buf];
-      for (int tok = 0; tok < x.ntok; ++tok) {
+      for (int tok = gi; tok < x.ntok; tok += kSelGroups) {
         const int t = x.t0 + tok;
         const int n = x.pos0 + tok + 1;  // valid keys 0..pos
         uint32_t* out = p.indices + static_cast<int64_t>(t) * p.k;
         if (n <= p.k) {
-          for (int key = st_id; key < n; key += kSelThreads) {
+          for (int key = st_id; key < n; key += kGrpThreads) {
             const uint32_t r = phys_of(pg, p.page_shift, key);
             if (r == 0xFFFFFFFFu) atomicOr(p.err, kErrPage);
             out[key] = r;
           }
-          for (int i = n + st_id; i < p.k; i += kSelThreads) out[i] = 0xFFFFFFFFu;
+          for (int i = n + st_id; i < p.k; i += kGrpThreads) out[i] = 0xFFFFFFFFu;
           if (st_id == 0) p.lens[t] = static_cast<uint32_t>(n);
         } else {
-          select_row(s, s.scores[buf] + tok * L, n, p.k, pg, p.page_shift, out, p.err);
+          select_row(sg, st_id, bar, s.scores[buf] + tok * L, n, p.k, s.tmin[buf][tok], s.tmax[buf][tok], pg,
+                     p.page_shift, out, p.err);
           if (st_id == 0) p.lens[t] = static_cast<uint32_t>(p.k);
         }
       }
-      named_bar_sync(kBarSel, kSelThreads);
+      named_bar_sync(bar, kGrpThreads);
       mbar_arrive(smem_u32(&s.bar_sfree[buf]));
     }
   }
