@@ -10,15 +10,24 @@
 //   * MMA 128 keys (M) x 256 (token, head) columns (N) x 128 depth (K),
 //     kind::f8f6f4 e4m3 x e4m3 -> f32 in TMEM; 4 instructions of K = 32.
 //     With H_idx = 64 one tile covers 4 tokens (256 / H_idx in general).
-//   * A work item is (sequence, token tile, key chunk).  Q and q_scale are
-//     loaded once per item; K tiles stream through a 4-stage TMA ring, one
-//     box per page (page_size >= 128: one box per tile), so the paged cache
-//     is read in place.  Key tiles wholly past the last token's position
-//     are not computed, only filled with -inf.
-//   * Two TMEM accumulators (2 x 256 columns) let the MMA of tile i+1 run
-//     while the epilogue warps drain tile i (each: one TMEM lane quarter x
-//     one column slice): relu, x q_scale, sum over the token's heads,
-//     x k_scale, causal -inf, coalesced f32 stores.  The
+//   * A work item is (sequence, token tile of up to 4 groups, key chunk).
+//     Q and q_scale are loaded once per item; K tiles stream through a
+//     4-stage TMA ring, one box per page (page_size >= 128: one box per
+//     tile), so the paged cache is read in place.  Each K tile serves every
+//     token group of the item (4 MMA tiles of N = 256): a K tile feeding
+//     only one group left the kernel bound by the L2 -> shared-memory
+//     stream of K (measured on the end-to-end chunk: 1 group 1.63 ms,
+//     2 groups 1.44, 4 groups 1.35).  Key tiles wholly past the last
+//     token's position are not computed, only filled with -inf.
+//   * Two TMEM accumulators (2 x 256 columns) let the MMA of one group run
+//     while the epilogue warps drain the previous one (each warp: one TMEM
+//     lane quarter x one 64-column slice, read 32 columns at a time): relu,
+//     x q_scale, sum over the token's heads in head order, x k_scale,
+//     causal -inf, coalesced f32 stores.  Sixteen epilogue warps at 32
+//     columns a load hide the TMEM load and FMA latencies that eight warps
+//     at 64 columns (168 registers a thread) did not (1.35 -> 1.18 ms);
+//     splitting a token's sum into independent chains, or pairing heads in
+//     f32x2 FMAs, measured no better at sixteen warps.  The
 //     item's page ids are staged in shared memory and each lane's k_scale
 //     is loaded two tiles ahead, so no L2 round trip sits in a tile's
 //     epilogue (measured: with the lookup inline, the epilogue waited on it
@@ -37,10 +46,10 @@ constexpr int kDepth = 128;
 constexpr int kBM = 128;      // keys per tile (MMA M)
 constexpr int kBN = 256;      // (token, head) columns per tile (MMA N)
 constexpr int kStages = 4;
+constexpr int kGroups = 4;    // token groups (MMA tiles of N = 256) sharing each K tile
 // Epilogue warps (a multiple of 4: one per TMEM lane quarter and column
-// slice).  Measured on the end-to-end chunk: 8 warps 1.67 ms, 16 warps
-// 1.94 ms.
-constexpr int kEpiThreads = 32 * 8;
+// slice).
+constexpr int kEpiThreads = 32 * 16;
 constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kSlices = kEpiThreads / 128;   // column slices; 4 TMEM lane quarters each
 constexpr int kSliceCols = kBN / kSlices;
@@ -64,9 +73,9 @@ struct Params {
 };
 
 struct __align__(1024) Smem {
-  uint8_t q[kBN * kDepth];            // SW128 K-major: 256 rows x 128 B
+  uint8_t q[kGroups][kBN * kDepth];   // SW128 K-major: 256 rows x 128 B per token group
   uint8_t k[kStages][kBM * kDepth];   // SW128 K-major: 128 rows x 128 B each
-  float qs[kBN];
+  float qs[kGroups * kBN];
   int pages[kMaxItemPages];           // page ids of the item's key chunk
   unsigned long long bar_q, bar_kfull[kStages], bar_kempty[kStages], bar_afull[2], bar_aempty[2], bar_drain;
   uint32_t tmem_base;
@@ -81,7 +90,8 @@ template <int HIDX>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const Params p) {
-  constexpr int TOK = kBN / HIDX;      // tokens per tile
+  constexpr int TOK = kBN / HIDX;      // tokens per group (one MMA tile)
+  constexpr int TOKI = kGroups * TOK;  // tokens per item
   constexpr int SLICE_TOK = kSliceCols / HIDX;  // tokens per epilogue column slice
   constexpr uint32_t IDESC = idesc_e4m3_f32(kBM, kBN, 0, 0);
 
@@ -100,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (b < p.B) {
         const int ql = p.cu_q[b + 1] - p.cu_q[b];
         const int kl = p.kv_len[b];
-        ntt = (ql + TOK - 1) / TOK;
+        ntt = (ql + TOKI - 1) / TOKI;
         nkc = (kl + CW - 1) / CW;
         n = (ql > 0 && kl >= ql && kl <= p.score_stride) ? ntt * nkc : 0;
         if (ql > 0 && (kl < ql || kl > p.score_stride)) atomicOr(p.err, kErrShape);
@@ -141,9 +151,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cu0 = p.cu_q[b];
   const int q_len = p.cu_q[b + 1] - cu0;
   const int kvl = p.kv_len[b];
-  const int t0 = cu0 + tt * TOK;
-  const int ntok = min(TOK, q_len - tt * TOK);
-  const int pos0 = kvl - q_len + tt * TOK;
+  const int t0 = cu0 + tt * TOKI;
+  const int ntok = min(TOKI, q_len - tt * TOKI);
+  const int pos0 = kvl - q_len + tt * TOKI;
+  const int ngroups = (ntok + TOK - 1) / TOK;  // groups holding tokens (MMA tiles per K tile)
   const int key_lo = kc * CW;
   const int key_hi = min(key_lo + CW, kvl);
   const int64_t cover_hi = (key_hi == kvl) ? p.score_stride : key_hi;  // last chunk also fills past kv_len
@@ -177,10 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int page_lo = key_lo >> p.page_shift;
   const int npg = min(kMaxItemPages, ((key_lo + CW - 1) >> p.page_shift) - page_lo + 1);
   if (warp >= 2) {
-    const int c = threadIdx.x - 64;  // column (token-in-tile, head)
-    if (c < kBN) {
-      const int tok = c / HIDX, h = c % HIDX;
-      s.qs[c] = (tok < ntok) ? p.q_scale[static_cast<int64_t>(t0 + tok) * HIDX + h] : 0.f;
+    const int c = threadIdx.x - 64;  // column (token-in-item, head)
+    for (int cc = c; cc < kGroups * kBN; cc += kEpiThreads) {
+      const int tok = cc / HIDX, h = cc % HIDX;
+      s.qs[cc] = (tok < ntok) ? p.q_scale[static_cast<int64_t>(t0 + tok) * HIDX + h] : 0.f;
     }
     for (int i = c; i < npg; i += kEpiThreads) {
       const int pg = page_lo + i;
@@ -197,8 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_tiles > 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      mbar_arrive_expect_tx(smem_u32(&s.bar_q), kBN * kDepth);
-      tma_load_2d(smem_u32(s.q), &tm_q, 0, t0 * HIDX, smem_u32(&s.bar_q));
+      mbar_arrive_expect_tx(smem_u32(&s.bar_q), ngroups * kBN * kDepth);
+      for (int g = 0; g < ngroups; ++g)
+        tma_load_2d(smem_u32(s.q[g]), &tm_q, 0, (t0 + g * TOK) * HIDX, smem_u32(&s.bar_q));
       const int nbox = kBM / p.box_rows;
       int issued = 0;
       for (int i = 0; i < n_tiles; ++i) {
@@ -237,23 +249,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_tiles > 0) {
       bool ok = mbar_wait(smem_u32(&s.bar_q), 0, p.err);
       s.q_landed = ok ? 1 : 0;
-      const uint32_t q_base = smem_u32(s.q);
       int landed = 0;
       for (int i = 0; ok && i < n_tiles; ++i) {
-        const int st = i % kStages, a = i & 1;
+        const int st = i % kStages;
         if (!mbar_wait(smem_u32(&s.bar_kfull[st]), (i / kStages) & 1, p.err)) break;
         landed = i + 1;
-        if (!mbar_wait(smem_u32(&s.bar_aempty[a]), ((i >> 1) & 1) ^ 1, p.err)) break;
-        tc_fence_after();
         const uint32_t k_base = smem_u32(s.k[st]);
+        // MMA tile m = (K tile i, group g) into accumulator m & 1
+        for (int g = 0; ok && g < ngroups; ++g) {
+          const int m = i * ngroups + g, a = m & 1;
+          if (!mbar_wait(smem_u32(&s.bar_aempty[a]), ((m >> 1) & 1) ^ 1, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t q_base = smem_u32(s.q[g]);
 #pragma unroll
-        for (int kk = 0; kk < kDepth / 32; ++kk) {
-          const uint64_t ad = make_sdesc(k_base + kk * 32, 16, 1024, kSwizzle128B);
-          const uint64_t bd = make_sdesc(q_base + kk * 32, 16, 1024, kSwizzle128B);
-          mma_f8f6f4_ss(tmem + a * kBN, ad, bd, IDESC, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kDepth / 32; ++kk) {
+            const uint64_t ad = make_sdesc(k_base + kk * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bd = make_sdesc(q_base + kk * 32, 16, 1024, kSwizzle128B);
+            mma_f8f6f4_ss(tmem + a * kBN, ad, bd, IDESC, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&s.bar_afull[a]));
         }
+        if (!ok) break;
         mma_commit(smem_u32(&s.bar_kempty[st]));
-        mma_commit(smem_u32(&s.bar_afull[a]));
       }
       s.k_landed = landed;
       // Make sure no MMA is still writing TMEM when the CTA tears down.
@@ -266,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;      // TMEM lanes this warp may access
     const int slice = ew >> 2;         // columns [slice*kSliceCols, +kSliceCols)
     const int row = quarter * 32 + lane;
-    const float* qs = s.qs + slice * kSliceCols;
+    const float* qs_slice = s.qs + slice * kSliceCols;
     // k_scale of this lane's key (physical row) in tile i, from the staged page ids
     auto load_ks = [&](int i) -> float {
       const int key = (kt_begin + i) * kBM + row;
@@ -277,50 +297,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       return (pid >= 0 && prow < p.phys_rows) ? __ldg(p.k_scale + prow) : 0.f;
     };
     float ks_next = load_ks(0), ks_next2 = load_ks(1);
-    for (int i = 0; i < n_tiles; ++i) {
-      const int a = i & 1;
+    bool eok = true;
+    for (int i = 0; eok && i < n_tiles; ++i) {
       const int kt = kt_begin + i;
       const int key = kt * kBM + row;
       const float ks = ks_next;
       ks_next = ks_next2;
       ks_next2 = load_ks(i + 2);
-      // warp-uniform: the tcgen05.ld below is warp-collective
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_afull[a]), (i >> 1) & 1, p.err))) break;
-      tc_fence_after();
-      float acc[SLICE_TOK];
+      for (int g = 0; g < ngroups; ++g) {
+        const int m = i * ngroups + g, a = m & 1;
+        const float* qs = qs_slice + g * kBN;
+        // warp-uniform: the tcgen05.ld below is warp-collective
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s.bar_afull[a]), (m >> 1) & 1, p.err))) {
+          eok = false;
+          break;
+        }
+        tc_fence_after();
+        float acc[SLICE_TOK];
 #pragma unroll
-      for (int j = 0; j < SLICE_TOK; ++j) acc[j] = 0.f;
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * kBN + slice * kSliceCols;
+        for (int j = 0; j < SLICE_TOK; ++j) acc[j] = 0.f;
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * kBN + slice * kSliceCols;
 #pragma unroll
-      for (int cb = 0; cb < kSliceCols; cb += 64) {
-        // two loads in flight per wait; each token's heads summed in head
-        // order.  (Measured on the end-to-end chunk, not kept: interleaving
-        // the slice's tokens as independent FMA chains, 1.68 vs 1.63 ms, and
-        // software-pipelining 32-column TMEM loads under the sums, 1.64 ms.)
-        uint32_t v[64];
-        tmem_ld32(taddr + cb, *reinterpret_cast<uint32_t(*)[32]>(v));
-        tmem_ld32(taddr + cb + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        tmem_wait_ld();
+        for (int cb = 0; cb < kSliceCols; cb += 32) {
+          uint32_t v[32];
+          tmem_ld32(taddr + cb, v);
+          tmem_wait_ld_regs(v);
 #pragma unroll
-        for (int j = 0; j < 64; j += 4) {
-          const float4 q4 = *reinterpret_cast<const float4*>(qs + cb + j);
-          const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
+          for (int j = 0; j < 32; j += 4) {
+            const float4 q4 = *reinterpret_cast<const float4*>(qs + cb + j);
+            const float qq[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int tj = (cb + j + u) / HIDX;
-            acc[tj] = fmaf(fmaxf(__uint_as_float(v[j + u]), 0.f), qq[u], acc[tj]);
+            for (int u = 0; u < 4; ++u) {
+              const int tj = (cb + j + u) / HIDX;
+              acc[tj] = fmaf(fmaxf(__uint_as_float(v[j + u]), 0.f), qq[u], acc[tj]);
+            }
           }
         }
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&s.bar_aempty[a]));
-      if (key >= key_lo && key < cover_hi) {
+        tc_fence_before();
+        mbar_arrive(smem_u32(&s.bar_aempty[a]));
+        if (key >= key_lo && key < cover_hi) {
 #pragma unroll
-        for (int j = 0; j < SLICE_TOK; ++j) {
-          const int tok = slice * SLICE_TOK + j;
-          if (tok < ntok) {
-            const float v = (key <= pos0 + tok) ? ks * acc[j] : -INFINITY;
-            p.scores[static_cast<int64_t>(t0 + tok) * p.score_stride + key] = v;
+          for (int j = 0; j < SLICE_TOK; ++j) {
+            const int tok = g * TOK + slice * SLICE_TOK + j;
+            if (tok < ntok) {
+              const float v = (key <= pos0 + tok) ? ks * acc[j] : -INFINITY;
+              p.scores[static_cast<int64_t>(t0 + tok) * p.score_stride + key] = v;
+            }
           }
         }
       }
@@ -347,6 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, kTmemCols);
 }
 
+static_assert(sizeof(Smem) + 1024 <= 232448, "indexer shared memory exceeds a CTA's 227 KB");
+
 template <int HIDX>
 static cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const Params& p, int grid,
                             cudaStream_t stream) {
@@ -366,7 +390,7 @@ smla_status_t launch_indexer(const uint8_t* q, const float* q_scale, const uint8
                              int64_t score_stride, unsigned* err, cudaStream_t stream) {
   using namespace idx;
   if (seqs.T == 0 || seqs.B == 0) return SMLA_OK;
-  const int tok = kBN / h_idx;
+  const int tok = kGroups * kBN / h_idx;
   const int box_rows = std::min(seqs.page_size, kBM);
   CUtensorMap tq, tk;
   if (!encode_tma_2d_u8(&tq, q, kDepth, static_cast<uint64_t>(seqs.T) * h_idx, kDepth, kBN))
