@@ -92,7 +92,8 @@ smla_status_t smla_indexer_scores(const uint8_t* q, const float* q_scale, const 
  *                        ties broken toward the lower logical key, emitted in
  *                        ascending logical-key order
  *   indices[t, len..k) = 0xFFFFFFFF
- *   scores   f32 [T, score_stride] (entries past pos(t) are not read)
+ *   scores   f32 [T, score_stride] (entries past pos(t) do not affect the
+ *            result; a row's last 16-byte load may read up to three of them)
  *   indices  u32 [T, k] (output), topk_lengths u32 [T] (output)
  * workspace: caller-owned device scratch of at least
  * smla_topk_workspace_size(T, score_stride, k) bytes (16-byte aligned; may
