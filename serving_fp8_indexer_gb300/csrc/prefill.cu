@@ -451,7 +451,10 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     mbar_init(smem_u32(&s.bar_qraw), 1);
     mbar_init(smem_u32(&s.bar_q), kSoftThreads);
     for (int i = 0; i < NST; ++i) {
-      mbar_init(smem_u32(&s.bar_kv_full[i]), kProdThreads);
+      // each producer thread arrives twice per block: once when it has issued
+      // its copies (releasing its s.srow / s.idx writes) and once, through
+      // cp.async.mbarrier.arrive.noinc, when those copies have landed
+      mbar_init(smem_u32(&s.bar_kv_full[i]), 2 * kProdThreads);
       for (int q = 0; q < kRowQ; ++q) mbar_init(smem_u32(&s.bar_kv_empty[i][q]), 1);
     }
     mbar_init(smem_u32(&s.bar_s_full), 1);
@@ -906,6 +909,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
                         (KVP == 2 ? mbar_wait(smem_u32(&s.bar_kv_split), g & 1, p.err)
                                   : mbar_wait(smem_u32(&s.bar_kv_full[g % NST]), (g / NST) & 1, p.err));
         if (!__all_sync(0xffffffffu, wt)) { ok = false; break; }
+        fence_proxy_async_smem();  // the producers' cp.async rows, seen through the barrier, before the MMAs read them
         tc_fence_after();  // after the softmax's tcgen05.ld of S
         const uint64_t slot_off = static_cast<uint64_t>(((g % NST) * KVP * kSlotBytes) >> 4);
         if (leader) {
@@ -956,6 +960,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
             ok = false;
             break;
           }
+          fence_proxy_async_smem();  // V rows landed by cp.async (ordered through the softmax's wait)
           tc_fence_after();  // after the softmax's TMEM reads and rescale of O^T
           if (leader) {
 #pragma unroll
@@ -1096,21 +1101,27 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
             }
           }
         }
+        if (KVP != 2) {
+          // The slot is full once every producer's copies have landed; the
+          // producers do not wait for that themselves but go on to the next
+          // block, so the gathers of both slots can be in flight at once.
+          // The QK issuer fences (async proxy) after its wait.
+          mbar_arrive(smem_u32(&s.bar_kv_full[slot]));
+          cp_async_mbar_arrive_noinc(smem_u32(&s.bar_kv_full[slot]));
+        }
         // the next block's row and scale load while this block's rows land
         if (pt < kBK && j + 1 < I.nblk) {
           load_row(j + 1);
           load_scale();
         }
-        cp_async_wait_all();
         if (KVP == 2) {
+          cp_async_wait_all();
           publish_quarter(kRowQ - 1);
-        } else {
-          fence_proxy_async_smem();
-          mbar_arrive(smem_u32(&s.bar_kv_full[slot]));
         }
       }
       gb += I.nblk;
     }
+    cp_async_wait_all();  // no copy is still landing when the CTA tears down
   }
 
   tc_fence_before();

@@ -148,6 +148,13 @@ SMLA_DEVICE_INLINE uint64_t make_policy_evict_first() {
   return pol;
 }
 SMLA_DEVICE_INLINE void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Arrive on the mbarrier once all of this thread's earlier cp.async copies
+// have landed, without waiting for them here; the arrival counts toward the
+// barrier's expected count (.noinc).  A consumer that reads the copied bytes
+// through the async proxy (tcgen05.mma) fences after its wait.
+SMLA_DEVICE_INLINE void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 SMLA_DEVICE_INLINE void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Waits until at most N of this thread's committed cp.async groups are pending.
 template <int N>
