@@ -998,6 +998,14 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
     setmaxnreg_dec<kLowRegs>();
     const int pt = threadIdx.x - kProdWarp0 * 32;
     const uint64_t keep = make_policy_evict_last();  // the latent pool stays in L2 over the q / out streams
+    // The gather threads: kGRows rows x kPieces 16-byte pieces at a time;
+    // thread pt copies piece pc of its rows (consecutive threads on
+    // consecutive pieces of a row).
+    constexpr int kPieces = 36 * EB;  // 16-byte pieces of a cache row
+    constexpr int kGRows = kProdThreads / kPieces;
+    constexpr int kGThreads = kGRows * kPieces;
+    const int pc = pt % kPieces, pr = pt / kPieces;
+    const uint8_t* src_c = p.latent + pc * 16;
     bool ok = true;
     int gb = 0;
     for (int w = blockIdx.x; ok && w < items; w += gridDim.x) {
@@ -1079,12 +1087,19 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         for (int q = 0; q < kRowQ; ++q) {
           if (q > 0 && ok) ok = mbar_wait(smem_u32(&s.bar_kv_empty[slot][q]), par, p.err);
           if (ok) {
-            constexpr int kPieces = 36 * EB;  // 16-byte pieces of a cache row
-#pragma unroll 2
-            for (int i = pt; i < 32 * kPieces; i += kProdThreads) {
-              const int row = 32 * q + i / kPieces, c = i % kPieces;
-              const uint32_t dst = smem_u32(s.kv[slot][0]) + (c >> 2) * kChunkBytes + row * 64 + sw64(row, c & 3);
-              cp_async16_hint(dst, p.latent + static_cast<int64_t>(s.idx[row]) * (kD * EB) + c * 16, keep);
+            // Thread pt < kGThreads copies piece pc of rows pr, pr + kGRows, ...
+            // of the quarter (pc and pr fixed per thread).
+            if (pt < kGThreads) {
+              const uint32_t cbase = smem_u32(s.kv[slot][0]) + (pc >> 2) * kChunkBytes;
+#pragma unroll
+              for (int k = 0; k < (32 + kGRows - 1) / kGRows; ++k) {
+                const int rq = pr + k * kGRows;
+                if (rq < 32) {
+                  const int row = 32 * q + rq;
+                  cp_async16_hint(cbase + row * 64 + sw64(row, pc & 3),
+                                  src_c + static_cast<int64_t>(s.idx[row]) * (kD * EB), keep);
+                }
+              }
             }
             if (KVP == 2 && pt < 32) {
               const int row = 32 * q + pt;
