@@ -658,6 +658,7 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
         {
           const float4* c4p = reinterpret_cast<const float4*>(s.cs + hb);
           const float4* m4p = reinterpret_cast<const float4*>(s.negm + hb);
+          float ym[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four independent max chains
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const float4 c = c4p[q], m = m4p[q];
@@ -666,9 +667,10 @@ __global__ void __launch_bounds__(threads_for(KVP), 1)
             for (int k = 0; k < 4; ++k) {
               const int h = 4 * q + k;
               y[h] = fmaf(y[h], SC == kUnit ? cc[k] : sr * cc[k], mm[k]);
-              ymax = fmaxf(ymax, y[h]);
+              ym[k] = fmaxf(ym[k], y[h]);
             }
           }
+          ymax = fmaxf(fmaxf(ym[0], ym[1]), fmaxf(ym[2], ym[3]));
         }
         if ((j + 1) * kBK > n_item && j * kBK + r >= n_item) {  // lanes past the token's keys (its last block only)
 #pragma unroll
