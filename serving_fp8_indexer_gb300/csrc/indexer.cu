@@ -322,6 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v[32];
           tmem_ld32(taddr + cb, v);
           tmem_wait_ld_regs(v);
+          if (cb + 32 == kSliceCols) {  // the accumulator is in registers: the MMA may reuse it
+            tc_fence_before();
+            mbar_arrive(smem_u32(&s.bar_aempty[a]));
+          }
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
             const float4 q4 = *reinterpret_cast<const float4*>(qs + cb + j);
@@ -333,8 +337,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&s.bar_aempty[a]));
         if (key >= key_lo && key < cover_hi) {
 #pragma unroll
           for (int j = 0; j < SLICE_TOK; ++j) {
