@@ -229,6 +229,13 @@ __device__ __forceinline__ void split_f16x2(uint32_t a, uint16_t& hi, uint16_t& 
   hi = f16x2_to_e4m3x2(h);
   lo = f16x2_to_e4m3x2(hsub2(a, h));
 }
+// The same split with hi rounded by the conversion itself (nearest even,
+// e4m3's subnormals included) and read back: three conversions a pair, no
+// integer operations.
+__device__ __forceinline__ void split_f16x2_cvt(uint32_t a, uint16_t& hi, uint16_t& lo) {
+  hi = f16x2_to_e4m3x2(a);
+  lo = f16x2_to_e4m3x2(hsub2(a, e4m3x2_to_f16x2(hi)));
+}
 __device__ __forceinline__ uint4 quant16(const float (&x)[16]) {
   uint32_t w[4];
 #pragma unroll
@@ -273,8 +280,8 @@ __device__ __forceinline__ void split_quarter(uint8_t* hi_buf, uint8_t* lo_buf, 
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         uint16_t ha, hb, la, lb;
-        split_f16x2(hmul2(e4m3x2_to_f16x2(static_cast<uint16_t>(wv[k] & 0xffffu)), r2), ha, la);
-        split_f16x2(hmul2(e4m3x2_to_f16x2(static_cast<uint16_t>(wv[k] >> 16)), r2), hb, lb);
+        split_f16x2_cvt(hmul2(e4m3x2_to_f16x2(static_cast<uint16_t>(wv[k] & 0xffffu)), r2), ha, la);
+        split_f16x2_cvt(hmul2(e4m3x2_to_f16x2(static_cast<uint16_t>(wv[k] >> 16)), r2), hb, lb);
         h[k] = static_cast<uint32_t>(ha) | (static_cast<uint32_t>(hb) << 16);
         l[k] = static_cast<uint32_t>(la) | (static_cast<uint32_t>(lb) << 16);
       }
