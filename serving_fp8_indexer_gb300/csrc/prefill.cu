@@ -219,19 +219,12 @@ __device__ __forceinline__ void split8(const float (&x)[8], uint2& hi, uint2& lo
   hi = make_uint2(h[0], h[1]);
   lo = make_uint2(l[0], l[1]);
 }
-// Splits f16x2 a into e4m3 hi + lo: hi = a rounded to e4m3's 3 mantissa
-// bits (nearest even, as integer operations on the f16 bits; exact in e4m3's
-// normal range), lo = a - hi (exact in f16).  Two conversions per pair.  (For
-// the softmax's P and the q split, where the issue rate binds rather than the
-// conversion rate, the conversion round trip in split16 / split8 measured faster.)
-__device__ __forceinline__ void split_f16x2(uint32_t a, uint16_t& hi, uint16_t& lo) {
-  const uint32_t h = (a + 0x003f003fu + ((a >> 7) & 0x00010001u)) & 0xff80ff80u;
-  hi = f16x2_to_e4m3x2(h);
-  lo = f16x2_to_e4m3x2(hsub2(a, h));
-}
-// The same split with hi rounded by the conversion itself (nearest even,
-// e4m3's subnormals included) and read back: three conversions a pair, no
-// integer operations.
+// Splits f16x2 a into e4m3 hi + lo: hi = a rounded to e4m3 by the conversion
+// (nearest even, e4m3's subnormals included) and read back, lo = a - hi
+// (exact in f16).  Three conversions a pair and no integer operations: the
+// blockwise split is bound by the ALU pipe (measured: rounding hi with
+// integer operations on the f16 bits, two conversions a pair, 4.93 ms
+// against 4.51 ms for this form on the blockwise workload).
 __device__ __forceinline__ void split_f16x2_cvt(uint32_t a, uint16_t& hi, uint16_t& lo) {
   hi = f16x2_to_e4m3x2(a);
   lo = f16x2_to_e4m3x2(hsub2(a, e4m3x2_to_f16x2(hi)));
@@ -250,30 +243,34 @@ __device__ __forceinline__ uint4 quant16(const float (&x)[16]) {
 // warp covers 8 rows x 4 pieces of one 64-byte chunk (512 contiguous bytes:
 // no bank conflicts).  x = e4m3 * (s_blk / s_row) in f16 (the product needs 8
 // significant bits, f16 keeps 11), hi = x rounded to e4m3's 3 mantissa bits
-// (nearest even, on the f16 bits), lo = x - hi (exact); hi overwrites the raw
-// piece, lo goes to the second buffer (split_f16x2).  bsc holds 18 block
-// scales per row, then 1 / s_row per row.
+// (nearest even), lo = x - hi (exact); hi overwrites the raw piece, lo goes
+// to the second buffer (split_f16x2_cvt).  bsc holds 18 block scales per
+// row, then 1 / s_row per row.  Piece i of the quarter is in row
+// 32q + ((i >> 2) & 31), 16-byte column c4 = i & 3 of chunk i >> 7; the
+// thread stride 256 keeps a thread's row and c4 and steps its chunk by 2.
 __device__ __forceinline__ void split_quarter(uint8_t* hi_buf, uint8_t* lo_buf, const float* bsc, int q) {
   // All of a thread's pieces are read first, then converted and written, so
   // that their conversion chains interleave (a piece is only ever read and
   // rewritten by its own thread).
   constexpr int kIt = (32 * 36 + kSoftThreads - 1) / kSoftThreads;
+  static_assert(kSoftThreads == 256, "a thread keeps its row and column; its chunk steps by 2");
+  const int row = 32 * q + ((threadIdx.x >> 2) & 31), c4 = threadIdx.x & 3, kc0 = threadIdx.x >> 7;
+  const uint32_t off0 = kc0 * kChunkBytes + row * 64 + sw64(row, c4);
+  const float* bs = bsc + row * kBlkScales + 2 * kc0 + (c4 >> 1);  // chunk kc0 + 2 it: block scale bs[4 it]
+  const float isr = bsc[kBK * kBlkScales + row];
   uint4 raw[kIt];
-  uint32_t off[kIt];
   float ratio[kIt];
 #pragma unroll
   for (int it = 0; it < kIt; ++it) {
-    const int i = threadIdx.x + it * kSoftThreads;
-    if (i < 32 * 36) {
-      const int kc = i >> 7, row = 32 * q + ((i >> 2) & 31), c4 = i & 3;
-      off[it] = kc * kChunkBytes + row * 64 + sw64(row, c4);
-      raw[it] = *reinterpret_cast<const uint4*>(hi_buf + off[it]);
-      ratio[it] = bsc[row * kBlkScales + 2 * kc + (c4 >> 1)] * bsc[kBK * kBlkScales + row];
+    if (threadIdx.x + it * kSoftThreads < 32 * 36) {
+      raw[it] = *reinterpret_cast<const uint4*>(hi_buf + off0 + it * (2 * kChunkBytes));
+      ratio[it] = bs[4 * it] * isr;
     }
   }
 #pragma unroll
   for (int it = 0; it < kIt; ++it) {
     if (threadIdx.x + it * kSoftThreads < 32 * 36) {
+      const uint32_t off = off0 + it * (2 * kChunkBytes);
       const uint32_t r2 = f32x2_to_f16x2(ratio[it], ratio[it]);
       const uint32_t wv[4] = {raw[it].x, raw[it].y, raw[it].z, raw[it].w};
       uint32_t h[4], l[4];
@@ -285,8 +282,8 @@ __device__ __forceinline__ void split_quarter(uint8_t* hi_buf, uint8_t* lo_buf, 
         h[k] = static_cast<uint32_t>(ha) | (static_cast<uint32_t>(hb) << 16);
         l[k] = static_cast<uint32_t>(la) | (static_cast<uint32_t>(lb) << 16);
       }
-      *reinterpret_cast<uint4*>(hi_buf + off[it]) = make_uint4(h[0], h[1], h[2], h[3]);
-      *reinterpret_cast<uint4*>(lo_buf + off[it]) = make_uint4(l[0], l[1], l[2], l[3]);
+      *reinterpret_cast<uint4*>(hi_buf + off) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(lo_buf + off) = make_uint4(l[0], l[1], l[2], l[3]);
     }
   }
 }
